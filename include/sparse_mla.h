@@ -1,0 +1,113 @@
+/*
+ * sparse_mla.h -- C ABI of the GB300 (sm_103a) sparse MLA attention forward (DSA top-k).
+ *
+ * The operation (FlashMLA PR #196, "Problem" and "Fix"; FlashMLA PR #216, "Summary";
+ * FlashMLA PR #198, "Summary" item 2):
+ *   For every query row t and head h, only the slots j of the row's index list that satisfy
+ *       j < L_t   and   0 <= indices[t][j] < s_kv
+ *   take part, where L_t = clamp(topk_length[t], 0, topk) when topk_length is given and
+ *   L_t = topk otherwise.  With K = kv[:, :d_qk] and V = kv[:, :d_v] (the same latent row),
+ *       logit_j   = sm_scale * <q[t,h,:], K[idx_j]>
+ *       m         = max_j logit_j                         -> max_logits[t,h]
+ *       lse[t,h]  = m + ln sum_j exp(logit_j - m)         (natural log, sink excluded)
+ *       O[t,h,:]  = sum_j exp(logit_j - m) V[idx_j] / (sum_j exp(logit_j - m)
+ *                                                      + [attn_sink] exp(attn_sink[h] - m))
+ *   A row without any counted slot yields O = 0, lse = +inf, max_logits = -inf, with or
+ *   without a sink.  Slots beyond L_t are never read, so their index values are unconstrained
+ *   (e.g. INT_MAX padding is fine).  A duplicated index counts once per slot.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers to contiguous row-major buffers.  The caller
+ *     owns every buffer; the library allocates nothing and keeps no pointer after the call.
+ *   - bf16 tensors are passed as `void*` holding IEEE bfloat16 values.
+ *   - The work is enqueued on `stream` and is asynchronous: a return value of SMLA_OK only
+ *     means the launch was accepted.  No launch happens when an error code is returned.
+ *   - s_q == 0 is a no-op that returns SMLA_OK (pointers are then not inspected).
+ *   - Supported shapes: h_q a positive multiple of 64 (<= 1024), d_qk in {512, 576},
+ *     d_v == 512, topk >= 1, sm_scale finite and > 0, s_q * h_q <= INT32_MAX.
+ *   - Alignment: q and kv (or kv_pool) 16-byte aligned; every other pointer 4-byte aligned.
+ *   - Requires an sm_103a device (GB300).
+ */
+#ifndef SPARSE_MLA_GB300_H_
+#define SPARSE_MLA_GB300_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMLA_ABI_VERSION 1
+
+typedef struct CUstream_st* smla_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  SMLA_OK = 0,
+  SMLA_ERR_NULL_PTR = 1,       /* a required pointer is NULL */
+  SMLA_ERR_BAD_SHAPE = 2,      /* a size or scalar argument is outside the supported set */
+  SMLA_ERR_MISALIGNED = 3,     /* a pointer violates the alignment rule above */
+  SMLA_ERR_LAUNCH = 4,         /* the CUDA launch (or a CUDA query) failed */
+  SMLA_ERR_DEVICE_TIMEOUT = 5, /* a device-side wait gave up (see sparse_mla_device_status) */
+  SMLA_ERR_TENSOR_MAP = 6      /* the TMA descriptor for an operand could not be encoded */
+} smla_status;
+
+/*
+ * Sparse MLA forward over one shared latent KV (FlashMLA PR #196, "Problem": the sparse
+ * prefill forward; one latent KV stream, h_kv = 1).
+ *   q            [s_q, h_q, d_qk]  bf16
+ *   kv           [s_kv, 1, d_qk]   bf16; V is kv[:, :, :d_v]
+ *   indices      [s_q, 1, topk]    int32; any value, -1 / <0 / >= s_kv mean "no key"
+ *   topk_length  [s_q]             int32 or NULL (FlashMLA PR #216, "Summary")
+ *   attn_sink    [h_q]             fp32 or NULL (logit units of sm_scale * q.k)
+ *   out          [s_q, h_q, d_v]   bf16   (written)
+ *   lse          [s_q, h_q]        fp32   (written)
+ *   max_logits   [s_q, h_q]        fp32   (written)
+ * When topk_length is NULL, each row's work is bounded by its last valid slot, found by a
+ * scan in the kernel prologue (FlashMLA PR #196, "Fix"); results are identical to passing
+ * that length explicitly.
+ */
+smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices,
+                           const int32_t* topk_length, const float* attn_sink, float sm_scale,
+                           int d_v, void* out, float* lse, float* max_logits, int64_t s_q,
+                           int64_t s_kv, int h_q, int d_qk, int topk, smla_stream_t stream);
+
+/*
+ * Same forward over a paged KV cache (FlashMLA PR #216, "Dynamic top-k": decode with
+ * per-request top-k token positions in a cache of 64-token pages).
+ *   kv_pool      [pool_rows, 1, d_qk] bf16; pool_rows = number of pages * page_block
+ *   block_table  [s_q / s_q_per_req, max_blocks] int32: page id of each page_block-token
+ *                block of every request; entries must name pages inside the pool
+ *   seqlens_k    [s_q / s_q_per_req] int32 KV length of each request, or NULL to use
+ *                s_kv_per_req for all requests
+ *   indices      [s_q, 1, topk] int32 token positions within the row's request
+ * Query row t belongs to request t / s_q_per_req (s_q must be a multiple of s_q_per_req).
+ * Position p of request b is read from pool row block_table[b][p / page_block] * page_block
+ * + p % page_block, and counts iff 0 <= p < seqlens_k[b] and p / page_block < max_blocks.
+ * All other arguments and outputs are as in sparse_mla_fwd.
+ */
+smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t pool_rows,
+                                 const int32_t* block_table, int max_blocks, int page_block,
+                                 const int32_t* seqlens_k, int64_t s_kv_per_req, int s_q_per_req,
+                                 const int32_t* indices, const int32_t* topk_length,
+                                 const float* attn_sink, float sm_scale, int d_v, void* out,
+                                 float* lse, float* max_logits, int64_t s_q, int h_q, int d_qk,
+                                 int topk, smla_stream_t stream);
+
+/*
+ * Reads (and, when reset != 0, clears) the device-side status word that kernels set when one
+ * of their bounded waits gave up: SMLA_OK or SMLA_ERR_DEVICE_TIMEOUT.  Synchronises with the
+ * device (a blocking copy of one int); SMLA_ERR_LAUNCH if that copy fails.
+ */
+smla_status sparse_mla_device_status(int reset);
+
+/* Static, human-readable description of a status code.  Never NULL. */
+const char* sparse_mla_status_string(smla_status status);
+
+/* SMLA_ABI_VERSION of the loaded library. */
+int sparse_mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MLA_GB300_H_ */

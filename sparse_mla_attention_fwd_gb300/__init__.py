@@ -1,0 +1,154 @@
+"""GB300-native sparse MLA attention forward (DeepSeek-style DSA top-k), sm_103a.
+
+Python names mirror the C ABI of include/sparse_mla.h.  Tensors are torch CUDA tensors (torch
+supplies device memory and streams only); outputs are allocated here when not given.
+
+    out, lse, max_logits = sparse_mla_fwd(q, kv, indices, topk_length=None, attn_sink=None,
+                                          sm_scale=None, d_v=512)
+
+Semantics (FlashMLA PR #196 "Problem"/"Fix", PR #216 "Summary", PR #198 "Summary" item 2): each
+query row attends to the slots j < L_t of its index list whose index lies in [0, s_kv); L_t is
+topk_length[t] clamped to [0, topk] when given, else topk.  O is bf16; lse (natural log, sink
+excluded) and max_logits (max of sm_scale * q.k) are fp32; a row without a counted slot gives
+O = 0, lse = +inf, max_logits = -inf.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from ._native import EXPORTED, SmlaError, load_library, status_string
+from .native_build import LIB_PATH, build as build_library
+
+__all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_device_status",
+           "sparse_mla_status_string", "SmlaError", "load_library", "build_library", "LIB_PATH"]
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def _check(t, name, dtype, device=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _outputs(q, h_q, d_v, out, lse, max_logits):
+    s_q = q.shape[0]
+    if out is None:
+        out = torch.empty((s_q, h_q, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=q.device)
+    if max_logits is None:
+        max_logits = torch.empty((s_q, h_q), dtype=torch.float32, device=q.device)
+    _check(out, "out", torch.bfloat16, q.device)
+    _check(lse, "lse", torch.float32, q.device)
+    _check(max_logits, "max_logits", torch.float32, q.device)
+    if tuple(out.shape) != (s_q, h_q, d_v) or tuple(lse.shape) != (s_q, h_q) \
+            or tuple(max_logits.shape) != (s_q, h_q):
+        raise ValueError("output tensors have the wrong shape")
+    return out, lse, max_logits
+
+
+def sparse_mla_fwd(q, kv, indices, topk_length=None, attn_sink=None, sm_scale=None, d_v=512,
+                   out=None, lse=None, max_logits=None, stream=None):
+    """q [s_q, h_q, d_qk] bf16; kv [s_kv, 1, d_qk] (or [s_kv, d_qk]) bf16; indices [s_q, 1, topk]
+    (or [s_q, topk]) int32; topk_length [s_q] int32 or None; attn_sink [h_q] fp32 or None.
+    Returns (out [s_q, h_q, d_v] bf16, lse [s_q, h_q] fp32, max_logits [s_q, h_q] fp32)."""
+    lib = load_library()
+    _check(q, "q", torch.bfloat16)
+    dev = q.device
+    _check(kv, "kv", torch.bfloat16, dev)
+    _check(indices, "indices", torch.int32, dev)
+    _check(topk_length, "topk_length", torch.int32, dev)
+    _check(attn_sink, "attn_sink", torch.float32, dev)
+    s_q, h_q, d_qk = q.shape
+    s_kv = kv.shape[0]
+    if kv.numel() != s_kv * d_qk:
+        raise ValueError("kv must be [s_kv, 1, d_qk] with the d_qk of q")
+    topk = indices.shape[-1] if indices.dim() else 0
+    if indices.numel() != s_q * topk:
+        raise ValueError("indices must be [s_q, 1, topk]")
+    if topk_length is not None and topk_length.numel() != s_q:
+        raise ValueError("topk_length must have s_q entries")
+    if attn_sink is not None and attn_sink.numel() != h_q:
+        raise ValueError("attn_sink must have h_q entries")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d_qk)
+    out, lse, max_logits = _outputs(q, h_q, d_v, out, lse, max_logits)
+    with torch.cuda.device(dev):
+        rc = lib.sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length), _ptr(attn_sink),
+                                float(sm_scale), int(d_v), _ptr(out), _ptr(lse), _ptr(max_logits),
+                                int(s_q), int(s_kv), int(h_q), int(d_qk), int(topk),
+                                _stream_handle(stream, dev))
+    if rc != 0:
+        raise SmlaError(rc, "sparse_mla_fwd")
+    return out, lse, max_logits
+
+
+def sparse_mla_fwd_paged(q, kv_pool, block_table, indices, page_block=64, seqlens_k=None,
+                         s_kv_per_req=None, s_q_per_req=1, topk_length=None, attn_sink=None,
+                         sm_scale=None, d_v=512, out=None, lse=None, max_logits=None, stream=None):
+    """Paged-KV variant: kv_pool [n_pages*page_block, 1, d_qk] bf16, block_table [n_req,
+    max_blocks] int32, seqlens_k [n_req] int32 or None (then every request has s_kv_per_req
+    tokens); indices hold token positions within the row's request."""
+    lib = load_library()
+    _check(q, "q", torch.bfloat16)
+    dev = q.device
+    _check(kv_pool, "kv_pool", torch.bfloat16, dev)
+    _check(block_table, "block_table", torch.int32, dev)
+    _check(indices, "indices", torch.int32, dev)
+    _check(seqlens_k, "seqlens_k", torch.int32, dev)
+    _check(topk_length, "topk_length", torch.int32, dev)
+    _check(attn_sink, "attn_sink", torch.float32, dev)
+    s_q, h_q, d_qk = q.shape
+    pool_rows = kv_pool.shape[0]
+    if kv_pool.numel() != pool_rows * d_qk:
+        raise ValueError("kv_pool must be [rows, 1, d_qk] with the d_qk of q")
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [n_req, max_blocks]")
+    max_blocks = block_table.shape[1]
+    if s_kv_per_req is None:
+        s_kv_per_req = max_blocks * page_block
+    topk = indices.shape[-1] if indices.dim() else 0
+    if indices.numel() != s_q * topk:
+        raise ValueError("indices must be [s_q, 1, topk]")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d_qk)
+    out, lse, max_logits = _outputs(q, h_q, d_v, out, lse, max_logits)
+    with torch.cuda.device(dev):
+        rc = lib.sparse_mla_fwd_paged(_ptr(q), _ptr(kv_pool), int(pool_rows), _ptr(block_table),
+                                      int(max_blocks), int(page_block), _ptr(seqlens_k),
+                                      int(s_kv_per_req), int(s_q_per_req), _ptr(indices),
+                                      _ptr(topk_length), _ptr(attn_sink), float(sm_scale), int(d_v),
+                                      _ptr(out), _ptr(lse), _ptr(max_logits), int(s_q), int(h_q),
+                                      int(d_qk), int(topk), _stream_handle(stream, dev))
+    if rc != 0:
+        raise SmlaError(rc, "sparse_mla_fwd_paged")
+    return out, lse, max_logits
+
+
+def sparse_mla_device_status(reset=False) -> int:
+    """Device-side status word (0, or 5 = a bounded wait gave up); synchronises."""
+    return int(load_library().sparse_mla_device_status(1 if reset else 0))
+
+
+def sparse_mla_status_string(code: int) -> str:
+    return status_string(code)

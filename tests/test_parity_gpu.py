@@ -1,0 +1,187 @@
+"""GPU parity: the CUDA path (through its C ABI) against the fp64 CPU oracle on the same seeded
+inputs, element by element at small sizes that span several 64-key blocks and ragged tails, and
+on sampled rows at the full configuration sizes.  Also the bit-level self-consistency the pages
+rely on: a run without topk_length equals a run with topk_length set to the derived length
+(FlashMLA PR #196, "Numbers": bitwise A/B of out / lse / max_logits)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_helpers import assert_parity, dev_tensor, run_gpu, run_oracle, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("with_len", [False, True])
+@pytest.mark.parametrize("with_sink", [False, True])
+def test_tiny_config_all_rows(with_len, with_sink):
+    w = W.tiny(with_len=with_len, with_sink=with_sink)
+    assert_parity(to_np(run_gpu(w)), run_oracle(w), f"tiny len={with_len} sink={with_sink}")
+
+
+CASES = [
+    # seed, s_q, s_kv, h_q, d_qk, topk
+    (1, 37, 300, 64, 512, 200),
+    (2, 21, 1000, 128, 576, 333),
+    (3, 16, 70, 64, 576, 64),
+    (4, 9, 5000, 128, 512, 1),
+    (5, 13, 129, 64, 512, 130),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"s{c[0]}" for c in CASES])
+@pytest.mark.parametrize("mode", ["plain", "len_poison", "sink_dup"])
+def test_random_shapes(case, mode):
+    seed, s_q, s_kv, h_q, d_qk, topk = case
+    w = W.random_case(seed, s_q, s_kv, h_q, d_qk, topk, with_len=(mode == "len_poison"),
+                      with_sink=(mode == "sink_dup"), poison_suffix=(mode == "len_poison"),
+                      dup=(mode == "sink_dup"))
+    assert_parity(to_np(run_gpu(w)), run_oracle(w), f"{case} {mode}")
+
+
+@pytest.mark.parametrize("case", CASES[:3], ids=[f"s{c[0]}" for c in CASES[:3]])
+def test_derived_length_is_bit_identical_to_passed_length(case):
+    seed, s_q, s_kv, h_q, d_qk, topk = case
+    w = W.random_case(seed, s_q, s_kv, h_q, d_qk, topk, with_sink=True)
+    L = oracle.last_valid_length(w["indices"], s_kv)
+    a = run_gpu(w, topk_length=None)
+    b = run_gpu(w, topk_length=L)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32))
+
+
+@pytest.mark.parametrize("tail", [0, 1, 17, 63, 64, 65, 127, 128])
+def test_tail_lengths(tail):
+    # FlashMLA PR #216, "Correctness": tail lengths 0,1,17,63,64,65,127,128 with the suffix
+    # after topk_length poisoned with INT_MAX.
+    rng = np.random.default_rng(100 + tail)
+    s_q, s_kv, h_q, d_qk, topk = 6, 600, 64, 576, 192
+    q = W.normal_bf16(rng, (s_q, h_q, d_qk))
+    kv = W.normal_bf16(rng, (s_kv, 1, d_qk))
+    idx = np.stack([rng.choice(s_kv, topk, replace=False) for _ in range(s_q)]).astype(np.int32)
+    L = np.full(s_q, tail, np.int32)
+    L[1] = min(tail + 1, topk)
+    idx_p = idx.copy()
+    for i in range(s_q):
+        idx_p[i, L[i]:] = W.INT_MAX
+    w = dict(q=q, kv=kv, indices=idx_p.reshape(s_q, 1, topk), topk_length=L, attn_sink=None,
+             sm_scale=float(np.float32(1 / np.sqrt(576))), d_v=512, paged=False)
+    gpu = run_gpu(w)
+    assert_parity(to_np(gpu), run_oracle(w), f"tail {tail}")
+    # same result as the -1 suffix without topk_length (bit-identical: same blocks, same order)
+    idx_m = idx.copy()
+    for i in range(s_q):
+        idx_m[i, L[i]:] = -1
+    w2 = dict(w, indices=idx_m.reshape(s_q, 1, topk), topk_length=None)
+    gpu2 = run_gpu(w2)
+    for i in range(s_q):
+        # the derived length equals L[i] only when slot L[i]-1 is valid (always, here)
+        assert torch.equal(gpu[0][i].view(torch.int16), gpu2[0][i].view(torch.int16))
+        assert torch.equal(gpu[1][i], gpu2[1][i]) and torch.equal(gpu[2][i], gpu2[2][i])
+
+
+def test_zero_rows_is_a_noop():
+    import sparse_mla_attention_fwd_gb300 as smla
+    q = torch.empty((0, 64, 512), dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros((10, 1, 512), dtype=torch.bfloat16, device="cuda")
+    idx = torch.zeros((0, 1, 8), dtype=torch.int32, device="cuda")
+    out, lse, mx = smla.sparse_mla_fwd(q, kv, idx)
+    assert out.shape == (0, 64, 512) and lse.shape == (0, 64)
+
+
+def test_empty_kv_gives_empty_rows():
+    w = W.random_case(9, 5, 40, 64, 512, 16)
+    w = dict(w, kv=w["kv"][:0], indices=w["indices"])
+    gpu = to_np(run_gpu(w))
+    assert np.all(gpu[0] == 0) and np.all(gpu[1] == np.inf) and np.all(gpu[2] == -np.inf)
+
+
+def test_single_valid_slot_is_bit_exact():
+    # one valid slot and no sink: O must be exactly that row's first d_v values
+    rng = np.random.default_rng(3)
+    s_q, s_kv = 8, 100
+    w = W.random_case(11, s_q, s_kv, 64, 576, 70)
+    idx = np.full((s_q, 1, 70), -1, np.int32)
+    pick = rng.integers(0, s_kv, size=s_q)
+    for i in range(s_q):
+        idx[i, 0, (7 * i) % 70] = pick[i]
+    w = dict(w, indices=idx, attn_sink=None, topk_length=None)
+    out = run_gpu(w)[0].view(torch.int16).cpu().numpy().view(np.uint16)
+    for i in range(s_q):
+        expect = w["kv"][pick[i], 0, :512]
+        assert np.array_equal(out[i], np.broadcast_to(expect, (64, 512)))
+
+
+# ---------------------------------------------------------------- full-size configurations
+SAMPLE = 48
+
+
+def _sampled_rows(s_q, extra=()):
+    rng = np.random.default_rng(1234)
+    rows = set(rng.choice(s_q, size=min(SAMPLE, s_q), replace=False).tolist())
+    rows.update([0, 1, s_q - 1])
+    rows.update(int(r) for r in extra)
+    return np.array(sorted(rows), np.int64)
+
+
+def _check_full(w, what, extra_rows=()):
+    s_q = w["q"].shape[0]
+    gpu = run_gpu(w)
+    rows = _sampled_rows(s_q, extra_rows)
+    assert_parity(to_np(gpu, rows), run_oracle(w, rows=rows), what)
+    # properties at every row: finite where the row has a counted slot, exact empties elsewhere
+    counts = W.valid_slot_count(w["indices"], w["s_kv"], w["topk_length"])
+    lse = gpu[1].cpu().numpy()
+    mx = gpu[2].cpu().numpy()
+    has = counts > 0
+    assert np.all(np.isfinite(lse[has])) and np.all(lse[~has] == np.inf)
+    assert np.all(mx[~has] == -np.inf)
+    assert bool(torch.isfinite(gpu[0].float()).all())
+    return gpu
+
+
+@pytest.mark.parametrize("with_len", [False, True])
+def test_ramp_config_sampled(with_len):
+    w = W.ramp(with_len=with_len)
+    _check_full(w, f"ramp len={with_len}")
+
+
+def test_ramp_len_vs_no_len_bit_identical():
+    w = W.ramp()
+    a = run_gpu(w, topk_length=None)
+    b = run_gpu(w, topk_length=w["valid_counts"])
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_full_config_sampled():
+    _check_full(W.full(), "full")
+
+
+def test_scattered_config_sampled():
+    w = W.scattered()
+    _check_full(w, "scattered", extra_rows=w["empty_rows"][:4])
+
+
+@pytest.mark.parametrize("dynamic", [True, False])
+def test_decode_config(dynamic):
+    w = W.decode(dynamic=dynamic)
+    gpu = run_gpu(w)
+    assert_parity(to_np(gpu), run_oracle(w), f"decode dynamic={dynamic}")
+
+
+def test_decode_fixed_equals_dynamic():
+    # FlashMLA PR #216 harness: fixed (-1 suffix, no topk_length) and dynamic (INT_MAX suffix,
+    # topk_length=1024) produce the same output
+    a = run_gpu(W.decode(dynamic=True))
+    b = run_gpu(W.decode(dynamic=False))
+    torch.testing.assert_close(a[0], b[0], atol=1e-3, rtol=2.01 / 128)
+    torch.testing.assert_close(a[1], b[1], atol=1e-6, rtol=8.01 / 65536)
+
+
+def test_no_device_timeouts_recorded():
+    import sparse_mla_attention_fwd_gb300 as smla
+    assert smla.sparse_mla_device_status() == 0
