@@ -1,0 +1,429 @@
+"""Benchmark of the sparse MLA forward on GB300.
+
+Default workload: the causal ramp-padded prefill (s_q=8192, s_kv=8192, h_q=64,
+d_qk=d_v=512, topk width 1152, row i holds min(i+1, 1027) valid indices, padded with -1),
+run WITHOUT topk_length -- the kernel derives each row's length itself.  One step = one call
+of the whole forward on that batch.  The metric is valid-token TFLOP/s,
+2*h_q*valid*(d_qk+d_v) summed over rows, divided by the device time of the call.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config ramp|full|scattered|decode|tiny]
+                  [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch of the same shape (weak
+scaling, no collective on the data path); the time is the max over ranks.
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "sparse-MLA fwd ms/call & valid-token TFLOP/s; % of GB300 bf16 tensor peak"
+UNIT = "TFLOP/s"
+# FlashMLA PR #196 "Numbers" (B200, not GB300): ramp-padded, no topk_length, 1.144 ms for
+# 1.0337 TFLOP of valid-token work -> 903.6 TFLOP/s.  Context only.
+PAGES_B200_TFLOPS = {("ramp", False): 1.0337e12 / 1.144e-3 / 1e12,
+                     ("ramp", True): 1.0337e12 / 1.101e-3 / 1e12}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=["ramp", "full", "scattered", "decode", "tiny"], default="ramp")
+    ap.add_argument("--with-len", action="store_true", help="pass topk_length in the timed steps")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--skip-cpu", action="store_true", help="no CPU-oracle baseline leg")
+    ap.add_argument("--skip-e2e", action="store_true", help="no host-buffer end-to-end leg")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def make_workload(name, with_len):
+    if name == "ramp":
+        return W.ramp(with_len=with_len)
+    if name == "full":
+        return W.full()
+    if name == "scattered":
+        return W.scattered()
+    if name == "decode":
+        return W.decode(dynamic=True)
+    return W.tiny(with_len=with_len, with_sink=True)
+
+
+def describe(w, name):
+    q = w["q"]
+    s_q, h_q, d_qk = q.shape
+    topk = w["indices"].reshape(s_q, -1).shape[1]
+    text = {
+        "ramp": f"causal ramp-padded prefill s_q={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} d_v=512 "
+                f"topk={topk} (row i: min(i+1,1027) valid, -1 padded)",
+        "full": f"fully-valid prefill s_q={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} d_v=512 topk={topk}",
+        "scattered": f"scattered-invalid prefill + sink s_q={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} "
+                     f"d_v=512 topk={topk} p_invalid=0.3",
+        "decode": f"paged decode B={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} d_v=512 topk={topk} "
+                  f"topk_length=1024 INT_MAX suffix, 64-token pages",
+        "tiny": f"tiny s_q={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} topk={topk}",
+    }[name]
+    return text
+
+
+def valid_flops(w, rows=None):
+    idx = w["indices"].reshape(w["q"].shape[0], -1)
+    tl = w["topk_length"]
+    if rows is not None:
+        idx = idx[rows]
+        tl = None if tl is None else np.asarray(tl)[rows]
+    counts = W.valid_slot_count(idx, w["s_kv"], tl)
+    h_q, d_qk = w["q"].shape[1], w["q"].shape[2]
+    return float(2.0 * h_q * counts.sum() * (d_qk + w["d_v"]))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("sparse_mla_attention_fwd_gb300/csrc/sparse_mla_fwd.cu",
+                "sparse_mla_attention_fwd_gb300/csrc/smla_ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config_name):
+    """DRAM bytes per launch from the committed ncu summary for this workload, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"sparse_mla_fwd_{config_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, enabled=True):
+        self.proc = None
+        self.gpu = gpu_index
+        if not enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except (ValueError, IndexError):
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """fp64 CPU oracle as the reference arm: each step is the oracle on a bounded sample of the
+    workload's rows, spread over the batch."""
+    if rank != 0:
+        return
+    import oracle
+
+    w = make_workload(args.config, args.with_len)
+    s_q = w["q"].shape[0]
+    cores = len(os.sched_getaffinity(0))
+    per_step = max(1, cores)
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        rows = rng.choice(s_q, size=min(per_step, s_q), replace=False)
+        _oracle_call(oracle, w, rows)
+    t_total, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        rows = rng.choice(s_q, size=min(per_step, s_q), replace=False)
+        t0 = time.perf_counter()
+        _oracle_call(oracle, w, rows)
+        t_total += time.perf_counter() - t0
+        flops += valid_flops(w, rows)
+    value = flops / t_total / 1e12
+    sample = f"{per_step} random rows per step of the {args.config} batch ({args.steps} steps)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": describe(w, args.config), "topk_length": "passed" if w["topk_length"] is not None else "omitted"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _oracle_call(oracle, w, rows):
+    if w.get("paged"):
+        return oracle.sparse_mla_fwd_paged(w["q"], w["kv"], w["block_table"], w["indices"], w["page_block"],
+                                           w.get("seqlens_k"), w["s_kv_per_req"], w["s_q_per_req"],
+                                           w["topk_length"], w["attn_sink"], w["sm_scale"], w["d_v"], rows=rows)
+    return oracle.sparse_mla_fwd(w["q"], w["kv"], w["indices"], w["topk_length"], w["attn_sink"],
+                                 w["sm_scale"], w["d_v"], rows=rows)
+
+
+def cpu_baseline(w, name, budget_s=12.0):
+    """The oracle as it stands, on a bounded row sample of the same workload."""
+    import oracle
+
+    s_q = w["q"].shape[0]
+    cores = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(1)
+    order = rng.permutation(s_q)
+    done, t_total, flops, pos = 0, 0.0, 0.0, 0
+    chunk = max(cores, 1)
+    while t_total < budget_s and pos < s_q:
+        rows = np.sort(order[pos:pos + chunk])
+        pos += chunk
+        t0 = time.perf_counter()
+        _oracle_call(oracle, w, rows)
+        t_total += time.perf_counter() - t0
+        flops += valid_flops(w, rows)
+        done += len(rows)
+    return {"value": flops / t_total / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} random rows of the {name} batch ({t_total:.1f} s of fp64 CPU work)"}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+
+    import sparse_mla_attention_fwd_gb300 as smla
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    w = make_workload(args.config, args.with_len)
+    s_q, h_q, d_qk = w["q"].shape
+    flops = valid_flops(w)
+
+    def host_tensor(a, pinned=True):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a)
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.pin_memory() if pinned else t
+
+    names = ["q", "kv", "indices", "topk_length", "attn_sink"]
+    if w.get("paged"):
+        names += ["block_table"]
+    host = {k: host_tensor(w.get(k)) for k in names}
+    devt = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    out = torch.empty((s_q, h_q, w["d_v"]), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((s_q, h_q), dtype=torch.float32, device=dev)
+    mx = torch.empty((s_q, h_q), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(d, tl="auto"):
+        t = d["topk_length"] if isinstance(tl, str) else tl
+        if w.get("paged"):
+            return smla.sparse_mla_fwd_paged(d["q"], d["kv"], d["block_table"], d["indices"],
+                                             page_block=w["page_block"], s_kv_per_req=w["s_kv_per_req"],
+                                             s_q_per_req=w["s_q_per_req"], topk_length=t,
+                                             attn_sink=d["attn_sink"], sm_scale=w["sm_scale"],
+                                             d_v=w["d_v"], out=out, lse=lse, max_logits=mx, stream=stream)
+        return smla.sparse_mla_fwd(d["q"], d["kv"], d["indices"], t, d["attn_sink"], sm_scale=w["sm_scale"],
+                                   d_v=w["d_v"], out=out, lse=lse, max_logits=mx, stream=stream)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+
+    def timed_steps(n, tl="auto"):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record(stream)
+            call(devt, tl)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    for _ in range(args.warmup):
+        call(devt)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.3 if not args.no_clocks else 0.0)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    step_ms = timed_steps(args.steps)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    total_ms = float(np.sum(step_ms))
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    launches = args.steps
+
+    # the same rows with topk_length passed (padding-overhead check), non-paged ramp only
+    extra = {}
+    if args.config == "ramp":
+        counts = torch.from_numpy(w["valid_counts"]).to(dev)
+        other = timed_steps(max(20, args.steps // 3), tl=(None if args.with_len else counts))
+        launches += len(other)
+        ms_other = float(np.mean(other))
+        ms_no_len, ms_len = (ms_other, ms_per_step) if args.with_len else (ms_per_step, ms_other)
+        extra = {"ms_no_topk_length": ms_no_len, "ms_topk_length_passed": ms_len,
+                 "padding_gap_pct": 100.0 * (ms_no_len - ms_len) / ms_len,
+                 "valid_token_tflop": flops / 1e12}
+
+    # end to end through the C ABI with host buffers: H2D of the inputs, the call, D2H of the
+    # outputs, all inside the timed region
+    e2e = None
+    if not args.skip_e2e:
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        mx_h = torch.empty(mx.shape, dtype=mx.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = sum(t.numel() * t.element_size() for t in (out, lse, mx))
+        e_ms = []
+        for i in range(args.e2e_steps + 2):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k, v in host.items():
+                if v is not None:
+                    devt[k].copy_(v, non_blocking=True)
+            call(devt)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            mx_h.copy_(mx, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                e_ms.append(a.elapsed_time(b))
+        launches_e2e = args.e2e_steps + 2
+        e2e = {"value": world * flops / (float(np.mean(e_ms)) * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": float(np.mean(e_ms))}
+        launches += launches_e2e
+
+    status = smla.sparse_mla_device_status()
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": profiled_traffic(args.config),
+            "peak_source": f"bf16_tflops burst ({src})", "kernel": "sparse_mla_fwd_kernel"}
+    base = PAGES_B200_TFLOPS.get((args.config, bool(args.with_len)))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": (value / base) if base else None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(w, args.config),
+                   "topk_length": "passed" if (args.with_len or w["topk_length"] is not None) else "omitted",
+                   "l2": "flushed (256 MB write) between timed iterations",
+                   "pct_of_bf16_peak": 100.0 * achieved / peak,
+                   "vs_baseline_ref": "FlashMLA PR #196 B200 number (other hardware, context)" if base else None},
+        "roofline": roof,
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "gpu_launches_total": launches,
+        "device_status": status,
+    }
+    line.update(extra)
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.skip_cpu and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.config)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
