@@ -4,20 +4,33 @@
 // (h_kv = 1; K = kv[:, :d_qk], V = kv[:, :d_v]).  A slot j counts iff j < L_t and
 // 0 <= idx[t][j] < s_kv, where L_t is the row's effective length: the caller's topk_length[t]
 // clamped to [0, topk], or, when no topk_length is given, one past the last valid slot found
-// by a tail scan in the prologue (FlashMLA PR #196, "Fix").  Rows with no valid slot return
-// O = 0, lse = +inf, max_logits = -inf (FlashMLA PR #196, "Correctness notes").  The optional
+// by a tail scan (FlashMLA PR #196, "Fix").  Rows with no valid slot return O = 0,
+// lse = +inf, max_logits = -inf (FlashMLA PR #196, "Correctness notes").  The optional
 // per-head attention sink is a value-less virtual key in the softmax denominator (FlashMLA
 // PR #198, "Summary" item 2).
 //
-// One CTA computes one (token, group of 64 heads).  Warp roles (288 threads):
-//   warps 0-3  producer : TMA gather4 of the selected KV rows into a 2-stage ring; slots that
-//                         are invalid or past L_t get an out-of-range row coordinate, so TMA
-//                         zero-fills them and their index is never used as an address
-//   warps 4-7  softmax  : online exp2 softmax on S (one head per TMEM lane), P -> smem,
-//                         lazy O rescale, epilogue (sink, normalise, write O / lse / max)
-//   warp  8    MMA      : TMEM allocation and tcgen05.mma issue (one elected thread)
+// Work item = (token, group of 64 heads).  The kernel is persistent: one CTA per SM walks a
+// static round-robin list of items, and every role streams through the same sequence of
+// 64-key blocks, so one item's tail overlaps the next item's head.
+//
+// Warp roles (512 threads, 16 warps):
+//   warps 0-7   gather     : TMA gather4 of the selected KV rows into a 2-stage ring.  A slot
+//                            that is invalid or past L_t carries row coordinate -1, so TMA
+//                            zero-fills it and its index is never used as an address.
+//   warps 8-11  softmax    : online exp2 softmax on S (one head per TMEM lane), P -> smem,
+//                            lazy O rescale, epilogue (sink, normalise, write O / lse / max).
+//   warp  12    MMA        : TMEM allocation and tcgen05.mma issue (one thread).
+//   warp  13    scheduler  : per item, derives L_t (topk_length or tail scan) and the block
+//                            count max(ceil(L_t/64), 1); per block, resolves the 64 slots to
+//                            row coordinates and a validity mask in a shared-memory ring.  It
+//                            runs ahead of the others, so index loads never sit on the
+//                            critical path; every role reads the same block count from the
+//                            ring, so the k-block loop bound is uniform.
+//   warp  14    Q loader   : TMA of each item's Q tile once the previous item's last S=QK^T
+//                            has been issued and completed.
+//   warp  15    idle.
 // Tensor-core work per 64-key block:
-//   S[64 heads x 64 keys]  = Q_g . K_blk^T        (M=64, N=64,  K=d_qk; both K-major SW128)
+//   S[64 heads x 64 keys]  = Q_g . K_blk^T        (M=64, N=64, K=d_qk; both K-major SW128)
 //   O^T[512 x 64 heads]   += V_blk^T . P^T        (4 x M=128, N=64, K=64; V^T read MN-major
 //                                                  straight out of the gathered K block)
 // TMEM: O^T in columns [0,256), S double buffer in [256,384).
@@ -39,19 +52,24 @@ namespace smla {
 namespace {
 
 constexpr int kBlockN = 64;            // keys per k-block
-constexpr int kGroupHeads = 64;        // heads per CTA
+constexpr int kGroupHeads = 64;        // heads per work item
 constexpr int kDv = 512;               // value width (first d_v columns of each kv row)
-constexpr int kThreads = 288;
-constexpr int kProducerThreads = 128;  // warps 0-3
-static_assert(kProducerThreads == 32 * 4, "producer warps precede the softmax warps");
-constexpr int kSoftmaxWarp0 = 4;       // warps 4-7
-constexpr int kMmaWarp = 8;
+constexpr int kThreads = 512;
+constexpr int kGatherWarps = 8;        // warps 0-7
+constexpr int kSoftmaxWarp0 = 8;       // warps 8-11
+constexpr int kMmaWarp = 12;
+constexpr int kSchedWarp = 13;
+constexpr int kQWarp = 14;
+constexpr int kRing = 8;               // scheduler ring depth (blocks)
+constexpr int kRingConsumers = kGatherWarps + 4 + 1;   // arrivals that free a ring slot
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O^T: 4 chunks x 64 columns
 constexpr uint32_t kTmemS = 256;       // S buffers: 256 + 64*b
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the running max grows by > 2^8
+
+enum : uint32_t { kFirstBlock = 1u, kLastBlock = 2u };
 
 __device__ int g_device_status = 0;    // SMLA_ERR_DEVICE_TIMEOUT once any wait gave up
 
@@ -68,6 +86,7 @@ struct FwdParams {
   int h_q;
   int topk;
   int n_groups;                // h_q / 64
+  int64_t n_items;             // s_q * n_groups
   // paged KV cache
   const int32_t* block_table;  // [n_req, max_blocks]
   const int32_t* seqlens_k;    // [n_req] or null
@@ -76,6 +95,14 @@ struct FwdParams {
   int s_q_per_req;
   int64_t pool_rows;           // rows the KV tensor map covers
   uint64_t wait_limit_ns;
+};
+
+// One 64-key block as resolved by the scheduler warp.
+struct BlockDesc {
+  int32_t rows[kBlockN];       // TMA row coordinate per slot, -1 when the slot does not count
+  uint32_t mask[2];            // validity bits of slots 0-31 / 32-63
+  int32_t item;                // work item this block belongs to
+  uint32_t flags;              // kFirstBlock | kLastBlock
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -91,6 +118,14 @@ __device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, vola
     *abort = 1;
     atomicExch(&g_device_status, static_cast<int>(SMLA_ERR_DEVICE_TIMEOUT));
   }
+}
+
+// Bounded wait that ignores the abort flag: used only to let this CTA's own asynchronous
+// copies / MMAs finish before it releases TMEM or exits.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  int never = 0;
+  if (!mbar_wait_bounded(bar, parity, &never, limit_ns))
+    atomicExch(&g_device_status, static_cast<int>(SMLA_ERR_DEVICE_TIMEOUT));
 }
 
 template <bool PAGED>
@@ -126,60 +161,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kChunks = D_QK / 64;                 // 128-byte column chunks of a row
   constexpr uint32_t kTileBytes = kChunks * 8192u;   // 64 rows x D_QK bf16 (= Q tile = stage)
   constexpr int kQkSteps = D_QK / 16;
+  // P^T (64 heads x 64 keys bf16, 8 KB) of block b lives in the rope chunk (columns 512..575)
+  // of stage b%2 when there is one -- that chunk is dead once S = QK^T has been computed --
+  // and in a separate double buffer otherwise.
+  constexpr bool kPInStage = (kChunks > 8);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + kTileBytes;                  // stage s at sKV + s * kTileBytes
-  uint8_t* sP = smem + 3 * kTileBytes;               // P as [64 heads][64 keys] bf16, SW128
+  uint8_t* sPbuf = smem + 3 * kTileBytes;            // used when !kPInStage: 2 x 8 KB
 
-  __shared__ __align__(8) uint64_t bar_q, bar_full[2], bar_empty[2], bar_s[2], bar_p, bar_o;
+  __shared__ __align__(16) BlockDesc ring[kRing];
+  __shared__ __align__(8) uint64_t bar_ring_full[kRing], bar_ring_empty[kRing];
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty;
+  __shared__ __align__(8) uint64_t bar_kv_full[2], bar_kv_empty[2];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2], bar_o_free, bar_final;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int s_last;
   __shared__ float s_alpha[kGroupHeads];
   __shared__ float s_inv[kGroupHeads];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) / p.n_groups;
-  const int g = static_cast<int>(static_cast<int64_t>(blockIdx.x) % p.n_groups);
-  const int topk = p.topk;
-  const int32_t* idx_row = p.indices + t * static_cast<int64_t>(topk);
-  const int64_t kv_len = row_kv_len<PAGED>(p, t);
   volatile int* abort = &abort_flag;
+  const uint64_t lim = p.wait_limit_ns;
+  // items of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int64_t n_my_items =
+      p.n_items > blockIdx.x ? (p.n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
-  // ---- prologue, part 1: issue the effective-length loads before any setup, so they are in
-  // flight while barriers are initialised, Q is requested and TMEM is allocated.
-  int my_last = -1;
-  int given_len = 0;
-  if (DYNAMIC) {
-    if (tid == 0) given_len = __ldg(p.topk_length + t);
-  } else {
-    for (int j = tid; j < topk; j += kThreads) {
-      const int v = __ldg(idx_row + j);
-      if (slot_ok<PAGED>(p, v, kv_len)) my_last = j;
-    }
-  }
+  auto p_addr = [&](int b) -> uint8_t* {
+    if constexpr (kPInStage) return sKV + (b & 1) * kTileBytes + 8 * 8192;
+    else return sPbuf + (b & 1) * 8192;
+  };
 
   if (tid == 0) {
     abort_flag = 0;
-    s_last = -1;
-    mbar_init(smem_u32(&bar_q), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_empty[s]), 1);
-      mbar_init(smem_u32(&bar_s[s]), 1);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(smem_u32(&bar_ring_full[r]), 1);
+      mbar_init(smem_u32(&bar_ring_empty[r]), kRingConsumers);
     }
-    mbar_init(smem_u32(&bar_p), 128);
-    mbar_init(smem_u32(&bar_o), 1);
+    mbar_init(smem_u32(&bar_q_full), 1);
+    mbar_init(smem_u32(&bar_q_empty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+      mbar_init(smem_u32(&bar_s_full[s]), 1);
+      mbar_init(smem_u32(&bar_p_full[s]), 128);
+      mbar_init(smem_u32(&bar_o_done[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_o_free), 128);
+    mbar_init(smem_u32(&bar_final), 1);
     fence_mbar_init();
-    // Q tile of this (token, head group): 64 rows of the [s_q*h_q, d_qk] view.
-    mbar_arrive_expect_tx(smem_u32(&bar_q), kTileBytes);
-    const int qrow = static_cast<int>(t * p.h_q + g * kGroupHeads);
-    for (int c = 0; c < kChunks; ++c)
-      tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, qrow, smem_u32(&bar_q));
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
@@ -188,51 +222,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-
-  // ---- prologue, part 2: consume.  Every warp then derives the same loop bound from the same
-  // value, so the k-block loop is uniform across all roles.
-  if (DYNAMIC) {
-    if (tid == 0) s_last = min(max(given_len, 0), topk) - 1;
-  } else {
-    int m = my_last;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0 && m >= 0) atomicMax(&s_last, m);
-  }
-  __syncthreads();
-  const int L = s_last + 1;
-  const int nblk = max((L + kBlockN - 1) / kBlockN, 1);
   const uint32_t tmem = tmem_slot;
 
-  if (warp < kSoftmaxWarp0) {
-    // ======================================================== producer: TMA gather
-    const int pi = tid;                 // 0..127
-    const int grp = pi & 15;            // 4-row group within the block
-    const int c0 = pi >> 4;             // column chunk 0..7
-    for (int k = 0; k < nblk; ++k) {
-      const int s = k & 1;
-      if (k >= 2) wait_or_flag(smem_u32(&bar_empty[s]), ((k >> 1) - 1) & 1, abort, p.wait_limit_ns);
-      if (pi == 0) mbar_arrive_expect_tx(smem_u32(&bar_full[s]), kTileBytes);
-      int rows[4];
+  if (warp == kSchedWarp) {
+    // ======================================================== scheduler
+    int64_t b = 0;
+    for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
+      const int64_t item = blockIdx.x + i * gridDim.x;
+      const int64_t t = item / p.n_groups;
+      const int32_t* idx_row = p.indices + t * static_cast<int64_t>(p.topk);
+      const int64_t kv_len = row_kv_len<PAGED>(p, t);
+      int L;
+      if (DYNAMIC) {
+        L = min(max(__ldg(p.topk_length + t), 0), p.topk);
+      } else {
+        // tail scan: one past the last slot that holds a valid index (FlashMLA PR #196, "Fix")
+        int last = -1;
+        for (int j = lane; j < p.topk; j += 32)
+          if (slot_ok<PAGED>(p, __ldg(idx_row + j), kv_len)) last = j;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = k * kBlockN + grp * 4 + i;
-        int coord = -1;                 // out of range: zero-filled, never read
-        if (j < L) {
-          const int v = __ldg(idx_row + j);
-          if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+        L = last + 1;
+      }
+      const int nblk = max((L + kBlockN - 1) / kBlockN, 1);
+      for (int k = 0; k < nblk && !*abort; ++k, ++b) {
+        const int r = static_cast<int>(b % kRing);
+        if (b >= kRing) wait_or_flag(smem_u32(&bar_ring_empty[r]), ((b / kRing) - 1) & 1, abort, lim);
+        uint32_t m[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int slot = k * kBlockN + 32 * h + lane;
+          int coord = -1;
+          if (slot < L) {
+            const int v = __ldg(idx_row + slot);
+            if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+          }
+          ring[r].rows[32 * h + lane] = coord;
+          m[h] = __ballot_sync(0xffffffffu, slot < L && coord >= 0);
         }
-        rows[i] = coord;
+        if (lane == 0) {
+          ring[r].mask[0] = m[0];
+          ring[r].mask[1] = m[1];
+          ring[r].item = static_cast<int32_t>(item);
+          ring[r].flags = (k == 0 ? kFirstBlock : 0u) | (k == nblk - 1 ? kLastBlock : 0u);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_ring_full[r]));
       }
-      uint8_t* st = sKV + s * kTileBytes;
-      const uint32_t bar = smem_u32(&bar_full[s]);
-      tma_gather4(smem_u32(st + c0 * 8192 + grp * 512), &kv_map, 64 * c0, rows[0], rows[1], rows[2],
-                  rows[3], bar);
-      if (kChunks > 8 && pi < 16 * (kChunks - 8)) {
-        const int c1 = 8 + (pi >> 4);
-        tma_gather4(smem_u32(st + c1 * 8192 + grp * 512), &kv_map, 64 * c1, rows[0], rows[1],
-                    rows[2], rows[3], bar);
+    }
+  } else if (warp == kQWarp) {
+    // ======================================================== Q loader
+    if (lane == 0) {
+      for (int64_t i = 0; i < n_my_items; ++i) {
+        const int64_t item = blockIdx.x + i * gridDim.x;
+        const int64_t t = item / p.n_groups;
+        const int g = static_cast<int>(item % p.n_groups);
+        if (i > 0) wait_or_flag(smem_u32(&bar_q_empty), (i - 1) & 1, abort, lim);
+        mbar_arrive_expect_tx(smem_u32(&bar_q_full), kTileBytes);
+        const int qrow = static_cast<int>(t * p.h_q + g * kGroupHeads);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, qrow, smem_u32(&bar_q_full));
+        if (*abort) break;
       }
+      // drain: the last Q tile has landed before this CTA may exit
+      if (n_my_items > 0) wait_drain(smem_u32(&bar_q_full), (n_my_items - 1) & 1, lim);
+    }
+  } else if (warp < kGatherWarps) {
+    // ======================================================== gather
+    const int pi = tid;                 // 0..255: one (4-row group, column chunk) item each
+    const int grp = pi & 15;
+    const int chunk = pi >> 4;
+    int64_t b = 0;
+    for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
+      for (bool more = true; more && !*abort; ++b) {
+        const int r = static_cast<int>(b % kRing);
+        const int s = static_cast<int>(b & 1);
+        wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
+        more = (ring[r].flags & kLastBlock) == 0;
+        if (b >= 2) wait_or_flag(smem_u32(&bar_kv_empty[s]), ((b >> 1) - 1) & 1, abort, lim);
+        if (pi == 0) mbar_arrive_expect_tx(smem_u32(&bar_kv_full[s]), kTileBytes);
+        if (chunk < kChunks) {
+          const int4 rr = *reinterpret_cast<const int4*>(&ring[r].rows[4 * grp]);
+          tma_gather4(smem_u32(sKV + s * kTileBytes + chunk * 8192 + grp * 512), &kv_map, 64 * chunk,
+                      rr.x, rr.y, rr.z, rr.w, smem_u32(&bar_kv_full[s]));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_ring_empty[r]));
+      }
+    }
+    // drain: the last fills of both stages have landed before this CTA may exit
+    if (pi == 0) {
+      for (int64_t bb = (b >= 2 ? b - 2 : 0); bb < b; ++bb)
+        wait_drain(smem_u32(&bar_kv_full[bb & 1]), (bb >> 1) & 1, lim);
     }
   } else if (warp < kMmaWarp) {
     // ======================================================== softmax / correction / epilogue
@@ -244,175 +325,244 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY;                    // running exponent offset (log2 units)
     float s_max = -INFINITY;                     // running max of raw q.k
     float l_sum = 0.f;
-
-    for (int k = 0; k < nblk; ++k) {
-      const int b = k & 1;
-      // validity of the block's 64 slots, from the indices (never from the gathered data)
-      const int ja = k * kBlockN + 2 * lane, jb = ja + 1;
-      bool oka = false, okb = false;
-      if (ja < L) oka = slot_ok<PAGED>(p, __ldg(idx_row + ja), kv_len);
-      if (jb < L) okb = slot_ok<PAGED>(p, __ldg(idx_row + jb), kv_len);
-      const uint32_t even_bits = __ballot_sync(0xffffffffu, oka);
-      const uint32_t odd_bits = __ballot_sync(0xffffffffu, okb);
-
-      wait_or_flag(smem_u32(&bar_s[b]), (k >> 1) & 1, abort, p.wait_limit_ns);
-      tc_fence_after();
-      float sv[kBlockN];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + kTmemS + 64 * b + 16 * i, r);
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) sv[16 * i + jj] = __uint_as_float(r[jj]);
-      }
-      tmem_ld_wait();
-
-      float alpha = 1.f;
-      bool need_rescale = false;
-      uint32_t pk[kBlockN / 2];
-      if (row_owner) {
-        float bm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kBlockN; ++j) {
-          const bool ok = ((((j & 1) ? odd_bits : even_bits) >> (j >> 1)) & 1u) != 0u;
-          sv[j] = ok ? sv[j] : -INFINITY;
-          bm = fmaxf(bm, sv[j]);
+    int64_t b = 0;
+    for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
+      for (bool more = true; more && !*abort; ++b) {
+        const int r = static_cast<int>(b % kRing);
+        const int sb = static_cast<int>(b & 1);
+        wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
+        const uint32_t mask_lo = ring[r].mask[0], mask_hi = ring[r].mask[1];
+        const uint32_t flags = ring[r].flags;
+        const int64_t item = ring[r].item;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_ring_empty[r]));
+        more = (flags & kLastBlock) == 0;
+        const bool first = (flags & kFirstBlock) != 0;
+        if (first) {
+          m_used = -INFINITY;
+          s_max = -INFINITY;
+          l_sum = 0.f;
         }
-        s_max = fmaxf(s_max, bm);
-        const float bm2 = bm * c;
-        if (bm2 > m_used + kRescaleLog2) {
-          alpha = fast_exp2(m_used - bm2);       // 0 when m_used was -inf
-          m_used = bm2;
-          need_rescale = true;
-        }
-        float ls = 0.f;
-#pragma unroll
-        for (int j = 0; j < kBlockN; j += 2) {
-          const float p0 = (sv[j] == -INFINITY) ? 0.f : fast_exp2(fmaf(sv[j], c, -m_used));
-          const float p1 = (sv[j + 1] == -INFINITY) ? 0.f : fast_exp2(fmaf(sv[j + 1], c, -m_used));
-          ls += p0 + p1;
-          pk[j >> 1] = pack_bf16x2(p0, p1);
-        }
-        l_sum = fmaf(l_sum, alpha, ls);
-      }
-      // O^T must be rescaled before PV(k) only if some head's offset moved and O already
-      // holds earlier blocks.
-      const bool any_rescale = named_bar_or(1, 128, need_rescale && k > 0);
-      // PV(k-1) must be complete before P is overwritten or O^T is touched.
-      if (k > 0) wait_or_flag(smem_u32(&bar_o), (k - 1) & 1, abort, p.wait_limit_ns);
-      if (any_rescale) {
-        if (row_owner) s_alpha[h] = alpha;
-        named_bar_sync(2, 128);
+
+        wait_or_flag(smem_u32(&bar_s_full[sb]), (b >> 1) & 1, abort, lim);
         tc_fence_after();
+        float sv[kBlockN];
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+          uint32_t rg[16];
+          tmem_ld16(tmem + lane_base + kTmemS + 64 * sb + 16 * i4, rg);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) sv[16 * i4 + jj] = __uint_as_float(rg[jj]);
+        }
+        tmem_ld_wait();
+
+        float alpha = 1.f;
+        bool need_rescale = false;
+        if (row_owner) {
+          float bm = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < kBlockN; ++j) {
+            const bool ok = (((j < 32 ? mask_lo : mask_hi) >> (j & 31)) & 1u) != 0u;
+            sv[j] = ok ? sv[j] : -INFINITY;
+            bm = fmaxf(bm, sv[j]);
+          }
+          s_max = fmaxf(s_max, bm);
+          const float bm2 = bm * c;
+          if (bm2 > m_used + kRescaleLog2) {
+            alpha = fast_exp2(m_used - bm2);       // 0 when m_used was -inf
+            m_used = bm2;
+            need_rescale = true;
+          }
+          // P row of head h as bf16 straight into the P^T operand tile ([64 heads][64 keys],
+          // 128-byte swizzle).  Its previous user (block b-2) finished its PV before the stage
+          // was refilled for block b, which S(b) being ready already implies.
+          uint8_t* prow = p_addr(static_cast<int>(b)) + h * 128;
+          float ls = 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 8 * u + 2 * e;
+              const float p0 = (sv[j] == -INFINITY) ? 0.f : fast_exp2(fmaf(sv[j], c, -m_used));
+              const float p1 = (sv[j + 1] == -INFINITY) ? 0.f : fast_exp2(fmaf(sv[j + 1], c, -m_used));
+              ls += p0 + p1;
+              w4[e] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(prow + ((u ^ (h & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          l_sum = fmaf(l_sum, alpha, ls);
+        }
+        // O^T holds earlier blocks of this item only when this is not the item's first block;
+        // it must then be rescaled before PV of this block if some head's offset moved.
+        const bool any_rescale = named_bar_or(1, 128, need_rescale && !first);
+        if (any_rescale) {
+          // PV of the previous block must be complete before O^T is touched
+          wait_or_flag(smem_u32(&bar_o_done[(b - 1) & 1]), ((b - 1) >> 1) & 1, abort, lim);
+          if (row_owner) s_alpha[h] = alpha;
+          named_bar_sync(2, 128);
+          tc_fence_after();
 #pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
+          for (int m = 0; m < 4; ++m) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t r[16];
-            const uint32_t addr = tmem + lane_base + kTmemO + 64 * m + 16 * i;
-            tmem_ld16(addr, r);
-            tmem_ld_wait();
+            for (int i4 = 0; i4 < 4; ++i4) {
+              uint32_t rg[16];
+              const uint32_t addr = tmem + lane_base + kTmemO + 64 * m + 16 * i4;
+              tmem_ld16(addr, rg);
+              tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              r[jj] = __float_as_uint(__uint_as_float(r[jj]) * s_alpha[16 * i + jj]);
-            tmem_st16(addr, r);
+              for (int jj = 0; jj < 16; ++jj)
+                rg[jj] = __float_as_uint(__uint_as_float(rg[jj]) * s_alpha[16 * i4 + jj]);
+              tmem_st16(addr, rg);
+            }
+          }
+          tmem_st_wait();
+          named_bar_sync(2, 128);                  // s_alpha is reused by the next rescale
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p_full[sb]));
+
+        if (!more) {
+          // ---- epilogue of this item
+          const int64_t t = item / p.n_groups;
+          const int g = static_cast<int>(item % p.n_groups);
+          const int head = g * kGroupHeads + h;
+          if (row_owner) {
+            const bool empty = !(l_sum > 0.f);
+            float den = l_sum;
+            if (p.attn_sink) den += exp2f(fmaf(__ldg(p.attn_sink + head), kLog2e, -m_used));
+            s_inv[h] = empty ? 0.f : 1.f / den;
+            const int64_t o = t * p.h_q + head;
+            p.lse[o] = empty ? INFINITY : (m_used + log2f(l_sum)) * kLn2;
+            p.max_logits[o] = empty ? -INFINITY : s_max * p.sm_scale;
+          }
+          wait_or_flag(smem_u32(&bar_o_done[sb]), (b >> 1) & 1, abort, lim);
+          named_bar_sync(2, 128);
+          tc_fence_after();
+          __nv_bfloat16* out_t = p.out + (t * p.h_q + g * kGroupHeads) * static_cast<int64_t>(kDv);
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+            __nv_bfloat16* dst = out_t + 128 * m + 32 * q + lane;   // column d of head 0
+#pragma unroll 1
+            for (int i4 = 0; i4 < 4; ++i4) {
+              uint32_t rg[16];
+              tmem_ld16(tmem + lane_base + kTmemO + 64 * m + 16 * i4, rg);
+              tmem_ld_wait();
+              if (m == 3 && i4 == 3) {
+                // all of O^T has been read: the next item's first PV may overwrite it
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bar_o_free));
+              }
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                const float inv = s_inv[16 * i4 + jj];
+                const float val = (inv == 0.f) ? 0.f : __uint_as_float(rg[jj]) * inv;
+                dst[(16 * i4 + jj) * kDv] = __float2bfloat16_rn(val);
+              }
+            }
           }
         }
-        tmem_st_wait();
-        named_bar_sync(2, 128);                  // s_alpha is reused next block
-      }
-      if (row_owner) {
-        uint8_t* row = sP + h * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          *reinterpret_cast<uint4*>(row + ((u ^ (h & 7)) << 4)) = v;
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p));
-    }
-
-    // ---- epilogue
-    wait_or_flag(smem_u32(&bar_o), (nblk - 1) & 1, abort, p.wait_limit_ns);
-    tc_fence_after();
-    const int head = g * kGroupHeads + h;
-    if (row_owner) {
-      const bool empty = !(l_sum > 0.f);
-      float den = l_sum;
-      if (p.attn_sink) den += exp2f(fmaf(__ldg(p.attn_sink + head), kLog2e, -m_used));
-      s_inv[h] = empty ? 0.f : 1.f / den;
-      const int64_t o = t * p.h_q + head;
-      p.lse[o] = empty ? INFINITY : (m_used + log2f(l_sum)) * kLn2;
-      p.max_logits[o] = empty ? -INFINITY : s_max * p.sm_scale;
-    }
-    named_bar_sync(2, 128);
-    __nv_bfloat16* out_t = p.out + (t * p.h_q + g * kGroupHeads) * static_cast<int64_t>(kDv);
-#pragma unroll 1
-    for (int m = 0; m < 4; ++m) {
-      const int d = 128 * m + 32 * q + lane;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + kTmemO + 64 * m + 16 * i, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int hh = 16 * i + jj;
-          const float inv = s_inv[hh];
-          const float val = (inv == 0.f) ? 0.f : __uint_as_float(r[jj]) * inv;
-          out_t[static_cast<int64_t>(hh) * kDv + d] = __float2bfloat16_rn(val);
-        }
       }
     }
-  } else {
+  } else if (warp == kMmaWarp) {
     // ======================================================== MMA issuer
     if (lane == 0) {
-      wait_or_flag(smem_u32(&bar_q), 0, abort, p.wait_limit_ns);
-      tc_fence_after();
       constexpr uint32_t idesc_qk = make_idesc_bf16(64, kBlockN, false, false);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, kGroupHeads, true, false);
       const uint32_t q_base = smem_u32(sQ);
       const uint32_t kv_base = smem_u32(sKV);
-      const uint32_t p_base = smem_u32(sP);
-      auto issue_pv = [&](int j) {
-        wait_or_flag(smem_u32(&bar_p), j & 1, abort, p.wait_limit_ns);
-        tc_fence_after();
-        const uint32_t st = kv_base + (j & 1) * kTileBytes;
+      // Blocks are issued in order.  S is double buffered, so QK(b) may run at most one block
+      // ahead of PV(b-1).  Both are polled: PV is issued as soon as its P is ready (it frees a
+      // KV stage for the gather warps), QK as soon as its stage has landed.
+      int64_t next_qk = 0, next_pv = 0;
+      int64_t qk_items = 0;                      // items whose last QK has been issued
+      int64_t pv_items = 0;                      // items whose last PV has been issued
+      uint32_t flags_even = 0u, flags_odd = 0u;  // ring flags of the blocks with QK issued
+      bool have_desc = false;
+      uint32_t desc_flags = 0u;
+      uint64_t t_progress = globaltimer_ns();
+      uint32_t spins = 0;
+      while (pv_items < n_my_items) {
+        if (*abort) break;
+        bool progressed = false;
+        if (next_pv < next_qk) {
+          const int sb = static_cast<int>(next_pv & 1);
+          const uint32_t fl = sb ? flags_odd : flags_even;
+          const bool first = (fl & kFirstBlock) != 0;
+          bool ok = mbar_test_wait(smem_u32(&bar_p_full[sb]), (next_pv >> 1) & 1);
+          if (ok && first && pv_items > 0) ok = mbar_test_wait(smem_u32(&bar_o_free), (pv_items - 1) & 1);
+          if (ok) {
+            tc_fence_after();
+            // descriptor start addresses advance in 16-byte units (low 14 bits)
+            const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
+            const uint64_t b0 = make_sdesc_sw128(smem_u32(p_addr(static_cast<int>(next_pv))), 16, 1024);
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-#pragma unroll
-          for (int ks = 0; ks < kBlockN / 16; ++ks) {
-            const uint64_t a = make_sdesc_sw128(st + (2 * m) * 8192 + ks * 2048, 8192, 1024);
-            const uint64_t bd = make_sdesc_sw128(p_base + ks * 32, 16, 1024);
-            umma_ss(tmem + kTmemO + 64 * m, a, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+              for (int ks = 0; ks < kBlockN / 16; ++ks) {
+                umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
+                        b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
+              }
+            }
+            umma_commit(smem_u32(&bar_kv_empty[sb]));
+            umma_commit(smem_u32(&bar_o_done[sb]));
+            if (fl & kLastBlock) ++pv_items;
+            ++next_pv;
+            progressed = true;
           }
         }
-        umma_commit(smem_u32(&bar_empty[j & 1]));
-        umma_commit(smem_u32(&bar_o));
-      };
-      for (int k = 0; k < nblk; ++k) {
-        const int s = k & 1;
-        wait_or_flag(smem_u32(&bar_full[s]), (k >> 1) & 1, abort, p.wait_limit_ns);
-        tc_fence_after();
-        const uint32_t st = kv_base + s * kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < kQkSteps; ++ks) {
-          const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-          umma_ss(tmem + kTmemS + 64 * s, make_sdesc_sw128(q_base + off, 16, 1024),
-                  make_sdesc_sw128(st + off, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
+        if (!progressed && next_qk <= next_pv + 1 && qk_items < n_my_items) {
+          const int r = static_cast<int>(next_qk % kRing);
+          if (!have_desc && mbar_test_wait(smem_u32(&bar_ring_full[r]), (next_qk / kRing) & 1)) {
+            desc_flags = ring[r].flags;
+            mbar_arrive(smem_u32(&bar_ring_empty[r]));
+            have_desc = true;
+          }
+          if (have_desc) {
+            const int s = static_cast<int>(next_qk & 1);
+            const bool first = (desc_flags & kFirstBlock) != 0;
+            bool ok = mbar_test_wait(smem_u32(&bar_kv_full[s]), (next_qk >> 1) & 1);
+            if (ok && first) ok = mbar_test_wait(smem_u32(&bar_q_full), qk_items & 1);
+            if (ok) {
+              tc_fence_after();
+              const uint64_t qd0 = make_sdesc_sw128(q_base, 16, 1024);
+              const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
+#pragma unroll 4
+              for (int ks = 0; ks < kQkSteps; ++ks) {
+                const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+                umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
+              }
+              umma_commit(smem_u32(&bar_s_full[s]));
+              if (desc_flags & kLastBlock) {
+                umma_commit(smem_u32(&bar_q_empty));
+                ++qk_items;
+              }
+              if (s) flags_odd = desc_flags;
+              else flags_even = desc_flags;
+              have_desc = false;
+              ++next_qk;
+              progressed = true;
+            }
+          }
         }
-        umma_commit(smem_u32(&bar_s[s]));
-        if (k > 0) issue_pv(k - 1);
+        if (progressed) {
+          t_progress = globaltimer_ns();
+          spins = 0;
+        } else if ((++spins & 63u) == 0u && globaltimer_ns() - t_progress > lim) {
+          *abort = 1;
+          atomicExch(&g_device_status, static_cast<int>(SMLA_ERR_DEVICE_TIMEOUT));
+        }
       }
-      issue_pv(nblk - 1);
+      // drain: every MMA issued above completes before TMEM is released
+      umma_commit(smem_u32(&bar_final));
+      wait_drain(smem_u32(&bar_final), 0, lim);
     }
     __syncwarp();
   }
 
-  // ---- teardown: every tcgen05 op has completed (the epilogue waited on the last PV commit,
-  // which tracks all earlier MMAs), so TMEM can be released.
+  // ---- teardown: every tcgen05 op has completed (each item's epilogue waited on its last PV
+  // commit, which tracks all earlier MMAs), so TMEM can be released.
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -451,15 +601,27 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 template <int D_QK, bool DYNAMIC, bool PAGED>
 smla_status launch_one(const CUtensorMap& qm, const CUtensorMap& kvm, const FwdParams& p,
                        cudaStream_t stream) {
   auto kern = sparse_mla_fwd_kernel<D_QK, DYNAMIC, PAGED>;
-  const size_t smem = 3 * (D_QK / 64) * 8192 + 8192 + 1024;
+  constexpr int kChunks = D_QK / 64;
+  const size_t smem = 3 * kChunks * 8192 + (kChunks > 8 ? 0 : 2 * 8192) + 1024;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return SMLA_ERR_LAUNCH;
-  const int64_t grid = p.s_q * p.n_groups;
+  const int sms = sm_count();
+  if (sms <= 0) return SMLA_ERR_LAUNCH;
+  // persistent: one CTA per SM (the shared-memory footprint admits only one), items assigned
+  // round-robin
+  const int64_t grid = p.n_items < sms ? p.n_items : sms;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(qm, kvm, p);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
 }
@@ -535,6 +697,7 @@ smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices
   p.h_q = h_q;
   p.topk = topk;
   p.n_groups = h_q / kGroupHeads;
+  p.n_items = s_q * p.n_groups;
   p.s_q_per_req = 1;
   p.page_block = 1;
   p.max_blocks = 1;
@@ -577,6 +740,7 @@ smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t poo
   p.h_q = h_q;
   p.topk = topk;
   p.n_groups = h_q / kGroupHeads;
+  p.n_items = s_q * p.n_groups;
   p.block_table = block_table;
   p.seqlens_k = seqlens_k;
   p.max_blocks = max_blocks;
