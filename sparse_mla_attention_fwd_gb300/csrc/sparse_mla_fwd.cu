@@ -73,6 +73,19 @@ enum : uint32_t { kFirstBlock = 1u, kLastBlock = 2u };
 
 __device__ int g_device_status = 0;    // SMLA_ERR_DEVICE_TIMEOUT once any wait gave up
 
+#ifdef SMLA_TRACE
+// Pipeline trace (debug builds only): SM clock stamps of each block's events in CTA 0.
+constexpr int kTraceBlocks = 256;
+enum TraceEvent { kTrRing, kTrGatherIssue, kTrQkIssue, kTrSReady, kTrPReady, kTrPvIssue, kTrEpilogue, kTrEvents };
+__device__ long long g_trace[kTraceBlocks][kTrEvents];
+__device__ __forceinline__ void trace(int64_t b, int ev) {
+  if (blockIdx.x == 0 && b < kTraceBlocks) g_trace[b][ev] = clock64();
+}
+#define SMLA_TRACE_EVENT(b, ev) trace((b), (ev))
+#else
+#define SMLA_TRACE_EVENT(b, ev) ((void)0)
+#endif
+
 struct FwdParams {
   const int32_t* indices;      // [s_q, topk]
   const int32_t* topk_length;  // [s_q] or null
@@ -267,7 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ring[r].flags = (k == 0 ? kFirstBlock : 0u) | (k == nblk - 1 ? kLastBlock : 0u);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_ring_full[r]));
+        if (lane == 0) {
+          SMLA_TRACE_EVENT(b, kTrRing);
+          mbar_arrive(smem_u32(&bar_ring_full[r]));
+        }
       }
     }
   } else if (warp == kQWarp) {
@@ -300,7 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
         more = (ring[r].flags & kLastBlock) == 0;
         if (b >= 2) wait_or_flag(smem_u32(&bar_kv_empty[s]), ((b >> 1) - 1) & 1, abort, lim);
-        if (pi == 0) mbar_arrive_expect_tx(smem_u32(&bar_kv_full[s]), kTileBytes);
+        if (pi == 0) {
+          SMLA_TRACE_EVENT(b, kTrGatherIssue);
+          mbar_arrive_expect_tx(smem_u32(&bar_kv_full[s]), kTileBytes);
+        }
         if (chunk < kChunks) {
           const int4 rr = *reinterpret_cast<const int4*>(&ring[r].rows[4 * grp]);
           tma_gather4(smem_u32(sKV + s * kTileBytes + chunk * 8192 + grp * 512), &kv_map, 64 * chunk,
@@ -346,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         wait_or_flag(smem_u32(&bar_s_full[sb]), (b >> 1) & 1, abort, lim);
         tc_fence_after();
+        if (q == 0 && lane == 0) SMLA_TRACE_EVENT(b, kTrSReady);
         float sv[kBlockN];
 #pragma unroll
         for (int i4 = 0; i4 < 4; ++i4) {
@@ -421,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
+        if (q == 0 && lane == 0) SMLA_TRACE_EVENT(b, kTrPReady);
         mbar_arrive(smem_u32(&bar_p_full[sb]));
 
         if (!more) {
@@ -440,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_or_flag(smem_u32(&bar_o_done[sb]), (b >> 1) & 1, abort, lim);
           named_bar_sync(2, 128);
           tc_fence_after();
+          if (q == 0 && lane == 0) SMLA_TRACE_EVENT(b, kTrEpilogue);
           __nv_bfloat16* out_t = p.out + (t * p.h_q + g * kGroupHeads) * static_cast<int64_t>(kDv);
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
@@ -494,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && first && pv_items > 0) ok = mbar_test_wait(smem_u32(&bar_o_free), (pv_items - 1) & 1);
           if (ok) {
             tc_fence_after();
+            SMLA_TRACE_EVENT(next_pv, kTrPvIssue);
             // descriptor start addresses advance in 16-byte units (low 14 bits)
             const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
             const uint64_t b0 = make_sdesc_sw128(smem_u32(p_addr(static_cast<int>(next_pv))), 16, 1024);
@@ -526,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && first) ok = mbar_test_wait(smem_u32(&bar_q_full), qk_items & 1);
             if (ok) {
               tc_fence_after();
+              SMLA_TRACE_EVENT(next_qk, kTrQkIssue);
               const uint64_t qd0 = make_sdesc_sw128(q_base, 16, 1024);
               const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
 #pragma unroll 4
@@ -775,5 +799,13 @@ const char* sparse_mla_status_string(smla_status s) {
 }
 
 int sparse_mla_abi_version(void) { return SMLA_ABI_VERSION; }
+
+#ifdef SMLA_TRACE
+// Debug builds only: copies the pipeline trace of CTA 0 ([256 blocks][7 events] int64 clock
+// stamps) into `dst` (host memory).
+int sparse_mla_trace_fetch(long long* dst) {
+  return cudaMemcpyFromSymbol(dst, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 }  // extern "C"
