@@ -13,22 +13,23 @@
 // static round-robin list of items, and every role streams through the same sequence of
 // 64-key blocks, so one item's tail overlaps the next item's head.
 //
-// Warp roles (512 threads, 16 warps):
-//   warps 0-7   gather     : TMA gather4 of the selected KV rows into a 2-stage ring.  A slot
-//                            that is invalid or past L_t carries row coordinate -1, so TMA
-//                            zero-fills it and its index is never used as an address.
-//   warps 8-11  softmax    : online exp2 softmax on S (one head per TMEM lane), P -> smem,
-//                            lazy O rescale, epilogue (sink, normalise, write O / lse / max).
-//   warp  12    MMA        : TMEM allocation and tcgen05.mma issue (one thread).
-//   warp  13    scheduler  : per item, derives L_t (topk_length or tail scan) and the block
-//                            count max(ceil(L_t/64), 1); per block, resolves the 64 slots to
-//                            row coordinates and a validity mask in a shared-memory ring.  It
-//                            runs ahead of the others, so index loads never sit on the
-//                            critical path; every role reads the same block count from the
-//                            ring, so the k-block loop bound is uniform.
-//   warp  14    Q loader   : TMA of each item's Q tile once the previous item's last S=QK^T
-//                            has been issued and completed.
-//   warp  15    idle.
+// Warp roles (384 threads, 12 warps = 3 per SM sub-partition, warp w on sub-partition w % 4):
+//   warps 0,1,3,8,9,11  gather    : TMA gather4 of the selected KV rows (whole rows: measured
+//                                   ~45% faster per byte than half rows) into a 2-stage ring.
+//                                   The 16 x (d_qk/64) gather4 ops of a block are dealt over
+//                                   the six warps (TMA issue rate grows with issuing warps).
+//                                   A slot that is invalid or past L_t carries row coordinate
+//                                   -1, so TMA zero-fills it and its index is never an address.
+//   warps 4-7           softmax   : online exp2 softmax on S read as 16x256b TMEM fragments
+//                                   (every lane holds 2 heads x 16 keys), P -> smem, lazy O
+//                                   rescale, epilogue (sink, normalise, write O / lse / max).
+//   warp 2              MMA       : TMEM allocation, Q tile loads, tcgen05.mma issue (one
+//                                   thread polling every readiness barrier without blocking).
+//   warp 10             scheduler : per item, derives L_t (topk_length or tail scan) and the
+//                                   block count max(ceil(L_t/64), 1); per block, resolves the 64
+//                                   slots to row coordinates and a validity mask in a shared
+//                                   ring.  It runs ahead, so index loads never sit on the
+//                                   critical path, and every role reads the same block count.
 // Tensor-core work per 64-key block:
 //   S[64 heads x 64 keys]  = Q_g . K_blk^T        (M=64, N=64, K=d_qk; both K-major SW128)
 //   O^T[512 x 64 heads]   += V_blk^T . P^T        (4 x M=128, N=64, K=64; V^T read MN-major
@@ -54,12 +55,14 @@ namespace {
 constexpr int kBlockN = 64;            // keys per k-block
 constexpr int kGroupHeads = 64;        // heads per work item
 constexpr int kDv = 512;               // value width (first d_v columns of each kv row)
-constexpr int kThreads = 512;
-constexpr int kGatherWarps = 8;        // warps 0-7
-constexpr int kSoftmaxWarp0 = 8;       // warps 8-11
-constexpr int kMmaWarp = 12;
-constexpr int kSchedWarp = 13;
-constexpr int kQWarp = 14;
+// 12 warps = 3 per SM sub-partition (warp w runs on sub-partition w % 4), so each thread may
+// hold up to 168 registers.  The MMA issuer and the scheduler share sub-partition 2 with one
+// softmax warp and no gather warp, whose TMA issue would compete with UMMA issue.
+constexpr int kThreads = 384;
+constexpr int kGatherWarps = 6;        // warps 0, 1, 3, 8, 9, 11
+constexpr int kSoftmaxWarp0 = 4;       // warps 4-7 (TMEM lane quadrants 0-3)
+constexpr int kMmaWarp = 2;            // also issues the Q tile loads
+constexpr int kSchedWarp = 10;
 constexpr int kRing = 8;               // scheduler ring depth (blocks)
 constexpr int kRingConsumers = kGatherWarps + 4 + 1;   // arrivals that free a ring slot
 constexpr uint32_t kTmemCols = 512;
@@ -67,7 +70,10 @@ constexpr uint32_t kTmemO = 0;         // O^T: 4 chunks x 64 columns
 constexpr uint32_t kTmemS = 256;       // S buffers: 256 + 64*b
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the running max grows by > 2^8
+constexpr float kRescaleLog2 = 8.0f;
+#ifndef SMLA_QK_LEAD
+#define SMLA_QK_LEAD 1
+#endif   // rescale O only when the running max grows by > 2^8
 
 enum : uint32_t { kFirstBlock = 1u, kLastBlock = 2u };
 
@@ -76,14 +82,22 @@ __device__ int g_device_status = 0;    // SMLA_ERR_DEVICE_TIMEOUT once any wait 
 #ifdef SMLA_TRACE
 // Pipeline trace (debug builds only): SM clock stamps of each block's events in CTA 0.
 constexpr int kTraceBlocks = 256;
-enum TraceEvent { kTrRing, kTrGatherIssue, kTrQkIssue, kTrSReady, kTrPReady, kTrPvIssue, kTrEpilogue, kTrEvents };
+enum TraceEvent {
+  kTrRing, kTrGatherIssue, kTrQkIssue, kTrSReady, kTrPReady, kTrPvIssue, kTrEpilogue,
+  kTrSLoaded, kTrSent, kTrRecv, kTrMath, kTrBar, kTrEvents
+};
 __device__ long long g_trace[kTraceBlocks][kTrEvents];
 __device__ __forceinline__ void trace(int64_t b, int ev) {
   if (blockIdx.x == 0 && b < kTraceBlocks) g_trace[b][ev] = clock64();
 }
 #define SMLA_TRACE_EVENT(b, ev) trace((b), (ev))
+#define SMLA_TRACE_EVENT_IF(cond, b, ev) \
+  do {                                   \
+    if (cond) trace((b), (ev));          \
+  } while (0)
 #else
 #define SMLA_TRACE_EVENT(b, ev) ((void)0)
+#define SMLA_TRACE_EVENT_IF(cond, b, ev) ((void)0)
 #endif
 
 struct FwdParams {
@@ -174,6 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kChunks = D_QK / 64;                 // 128-byte column chunks of a row
   constexpr uint32_t kTileBytes = kChunks * 8192u;   // 64 rows x D_QK bf16 (= Q tile = stage)
   constexpr int kQkSteps = D_QK / 16;
+  constexpr int kQkSlice = kQkSteps;                // QK k-steps issued per polling step
+  // QK(b) may be issued once PV(b - kQkLead) has been.  1 (measured best): S of the next
+  // block is computed while this block's softmax runs; 0 = strict QK(b), PV(b), QK(b+1).
+  constexpr int kQkLead = SMLA_QK_LEAD;
   // P^T (64 heads x 64 keys bf16, 8 KB) of block b lives in the rope chunk (columns 512..575)
   // of stage b%2 when there is one -- that chunk is dead once S = QK^T has been computed --
   // and in a separate double buffer otherwise.
@@ -286,28 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kQWarp) {
-    // ======================================================== Q loader
-    if (lane == 0) {
-      for (int64_t i = 0; i < n_my_items; ++i) {
-        const int64_t item = blockIdx.x + i * gridDim.x;
-        const int64_t t = item / p.n_groups;
-        const int g = static_cast<int>(item % p.n_groups);
-        if (i > 0) wait_or_flag(smem_u32(&bar_q_empty), (i - 1) & 1, abort, lim);
-        mbar_arrive_expect_tx(smem_u32(&bar_q_full), kTileBytes);
-        const int qrow = static_cast<int>(t * p.h_q + g * kGroupHeads);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, qrow, smem_u32(&bar_q_full));
-        if (*abort) break;
-      }
-      // drain: the last Q tile has landed before this CTA may exit
-      if (n_my_items > 0) wait_drain(smem_u32(&bar_q_full), (n_my_items - 1) & 1, lim);
-    }
-  } else if (warp < kGatherWarps) {
+  } else if (warp < kSoftmaxWarp0 && warp != kMmaWarp || warp >= kSoftmaxWarp0 + 4) {
     // ======================================================== gather
-    const int pi = tid;                 // 0..255: one (4-row group, column chunk) item each
-    const int grp = pi & 15;
-    const int chunk = pi >> 4;
+    // TMA issue throughput grows with the number of issuing warps, so the 16*kChunks gather4
+    // items of a block are dealt round-robin over the 6 gather warps.
+    const int gw = warp < 2 ? warp : (warp == 3 ? 2 : (warp < kSchedWarp ? warp - 5 : 5));   // 0..5
+    const int it = gw + kGatherWarps * lane;                  // item: (4-row group, column chunk)
+    const int grp = it & 15;
+    const int chunk = it >> 4;
+    const int pi = tid;
     int64_t b = 0;
     for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
       for (bool more = true; more && !*abort; ++b) {
@@ -334,16 +339,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t bb = (b >= 2 ? b - 2 : 0); bb < b; ++bb)
         wait_drain(smem_u32(&bar_kv_full[bb & 1]), (bb >> 1) & 1, lim);
     }
-  } else if (warp < kMmaWarp) {
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
     // ======================================================== softmax / correction / epilogue
     const int q = warp - kSoftmaxWarp0;          // TMEM lane quadrant 0..3
-    const bool row_owner = lane < 16;            // M=64 layout: heads live in lanes 0-15
-    const int h = 16 * q + lane;                 // local head (valid when row_owner)
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // 16x256b fragments of S (M=64 layout: heads 16q..16q+15 in lanes 0-15 of quadrant q):
+    // this thread holds heads hA = 16q + lane/4 and hB = hA + 8, columns 8i + 2(lane&3) + {0,1}.
+    const int hA = 16 * q + (lane >> 2);
+    const int hB = hA + 8;
+    const int cpair = 2 * (lane & 3);
+    const bool quad_leader = (lane & 3) == 0;
     const float c = p.sm_scale * kLog2e;
-    float m_used = -INFINITY;                    // running exponent offset (log2 units)
-    float s_max = -INFINITY;                     // running max of raw q.k
-    float l_sum = 0.f;
+    float m_used[2] = {-INFINITY, -INFINITY};    // running exponent offsets (log2 units)
+    float s_max[2] = {-INFINITY, -INFINITY};     // running max of raw q.k
+    float l_sum[2] = {0.f, 0.f};
     int64_t b = 0;
     for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
       for (bool more = true; more && !*abort; ++b) {
@@ -358,60 +367,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         more = (flags & kLastBlock) == 0;
         const bool first = (flags & kFirstBlock) != 0;
         if (first) {
-          m_used = -INFINITY;
-          s_max = -INFINITY;
-          l_sum = 0.f;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            m_used[x] = -INFINITY;
+            s_max[x] = -INFINITY;
+            l_sum[x] = 0.f;
+          }
         }
 
         wait_or_flag(smem_u32(&bar_s_full[sb]), (b >> 1) & 1, abort, lim);
         tc_fence_after();
-        if (q == 0 && lane == 0) SMLA_TRACE_EVENT(b, kTrSReady);
-        float sv[kBlockN];
+        SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrSReady);
+        float sv[32];   // sv[4i+0/1] = head hA, cols 8i+cpair+0/1; sv[4i+2/3] = head hB
 #pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4) {
-          uint32_t rg[16];
-          tmem_ld16(tmem + lane_base + kTmemS + 64 * sb + 16 * i4, rg);
+        for (int i8 = 0; i8 < 8; ++i8) {
+          uint32_t r4[4];
+          tmem_ld_16x256b(tmem + lane_base + kTmemS + 64 * sb + 8 * i8, r4);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) sv[16 * i4 + jj] = __uint_as_float(rg[jj]);
+          for (int e = 0; e < 4; ++e) sv[4 * i8 + e] = __uint_as_float(r4[e]);
         }
         tmem_ld_wait();
 
-        float alpha = 1.f;
-        bool need_rescale = false;
-        if (row_owner) {
-          float bm = -INFINITY;
+        if ((mask_lo & mask_hi) != 0xffffffffu) {
+          // this thread's columns are 8i + cpair + {0,1}: shift its bits down once
+          const uint32_t mlo = mask_lo >> cpair, mhi = mask_hi >> cpair;
 #pragma unroll
-          for (int j = 0; j < kBlockN; ++j) {
-            const bool ok = (((j < 32 ? mask_lo : mask_hi) >> (j & 31)) & 1u) != 0u;
-            sv[j] = ok ? sv[j] : -INFINITY;
-            bm = fmaxf(bm, sv[j]);
+          for (int i8 = 0; i8 < 8; ++i8) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const bool ok = (((i8 < 4 ? mlo : mhi) >> (8 * (i8 & 3) + e)) & 1u) != 0u;
+              sv[4 * i8 + e] = ok ? sv[4 * i8 + e] : -INFINITY;
+              sv[4 * i8 + 2 + e] = ok ? sv[4 * i8 + 2 + e] : -INFINITY;
+            }
           }
-          s_max = fmaxf(s_max, bm);
-          const float bm2 = bm * c;
-          if (bm2 > m_used + kRescaleLog2) {
-            alpha = fast_exp2(m_used - bm2);       // 0 when m_used was -inf
-            m_used = bm2;
+        }
+        float bm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int i8 = 0; i8 < 8; ++i8) {
+          bm[0] = fmaxf(bm[0], fmaxf(sv[4 * i8], sv[4 * i8 + 1]));
+          bm[1] = fmaxf(bm[1], fmaxf(sv[4 * i8 + 2], sv[4 * i8 + 3]));
+        }
+        float alpha[2] = {1.f, 1.f};
+        bool need_rescale = false;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          bm[x] = fmaxf(bm[x], __shfl_xor_sync(0xffffffffu, bm[x], 1));
+          bm[x] = fmaxf(bm[x], __shfl_xor_sync(0xffffffffu, bm[x], 2));
+          s_max[x] = fmaxf(s_max[x], bm[x]);
+          const float bm2 = bm[x] * c;
+          if (bm2 > m_used[x] + kRescaleLog2) {
+            alpha[x] = fast_exp2(m_used[x] - bm2);   // 0 when m_used was -inf
+            m_used[x] = bm2;
             need_rescale = true;
           }
-          // P row of head h as bf16 straight into the P^T operand tile ([64 heads][64 keys],
-          // 128-byte swizzle).  Its previous user (block b-2) finished its PV before the stage
-          // was refilled for block b, which S(b) being ready already implies.
-          uint8_t* prow = p_addr(static_cast<int>(b)) + h * 128;
-          float ls = 0.f;
+        }
+        // P as bf16 into the P^T operand tile ([64 heads][64 keys], 128-byte swizzle).  Its
+        // previous user (block b-2) finished its PV before the stage was refilled for block b,
+        // which S(b) being ready already implies.  Masked slots hold -inf and give
+        // exp2(-inf) = 0; a row whose offset is still -inf has no valid slot yet, and any finite
+        // offset then yields 0 as well.
+        const float neg_m0 = m_used[0] == -INFINITY ? 0.f : -m_used[0];
+        const float neg_m1 = m_used[1] == -INFINITY ? 0.f : -m_used[1];
+        uint8_t* ptile = p_addr(static_cast<int>(b));
+        uint8_t* prowA = ptile + hA * 128 + 2 * cpair;
+        uint8_t* prowB = ptile + hB * 128 + 2 * cpair;
+        const int swA = hA & 7, swB = hB & 7;
+        float ls[2] = {0.f, 0.f};
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint32_t w4[4];
+        for (int i8 = 0; i8 < 8; ++i8) {
+          const float p0 = fast_exp2(fmaf(sv[4 * i8], c, neg_m0));
+          const float p1 = fast_exp2(fmaf(sv[4 * i8 + 1], c, neg_m0));
+          const float p2 = fast_exp2(fmaf(sv[4 * i8 + 2], c, neg_m1));
+          const float p3 = fast_exp2(fmaf(sv[4 * i8 + 3], c, neg_m1));
+          ls[0] += p0 + p1;
+          ls[1] += p2 + p3;
+          *reinterpret_cast<uint32_t*>(prowA + ((i8 ^ swA) << 4)) = pack_bf16x2(p0, p1);
+          *reinterpret_cast<uint32_t*>(prowB + ((i8 ^ swB) << 4)) = pack_bf16x2(p2, p3);
+        }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 8 * u + 2 * e;
-              const float p0 = (sv[j] == -INFINITY) ? 0.f : fast_exp2(fmaf(sv[j], c, -m_used));
-              const float p1 = (sv[j + 1] == -INFINITY) ? 0.f : fast_exp2(fmaf(sv[j + 1], c, -m_used));
-              ls += p0 + p1;
-              w4[e] = pack_bf16x2(p0, p1);
-            }
-            *reinterpret_cast<uint4*>(prow + ((u ^ (h & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
-          l_sum = fmaf(l_sum, alpha, ls);
+        for (int x = 0; x < 2; ++x) {
+          ls[x] += __shfl_xor_sync(0xffffffffu, ls[x], 1);
+          ls[x] += __shfl_xor_sync(0xffffffffu, ls[x], 2);
+          l_sum[x] = fmaf(l_sum[x], alpha[x], ls[x]);
         }
         // O^T holds earlier blocks of this item only when this is not the item's first block;
         // it must then be rescaled before PV of this block if some head's offset moved.
@@ -419,7 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (any_rescale) {
           // PV of the previous block must be complete before O^T is touched
           wait_or_flag(smem_u32(&bar_o_done[(b - 1) & 1]), ((b - 1) >> 1) & 1, abort, lim);
-          if (row_owner) s_alpha[h] = alpha;
+          if (quad_leader) {
+            s_alpha[hA] = alpha[0];
+            s_alpha[hB] = alpha[1];
+          }
           named_bar_sync(2, 128);
           tc_fence_after();
 #pragma unroll 1
@@ -441,27 +481,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if (q == 0 && lane == 0) SMLA_TRACE_EVENT(b, kTrPReady);
+        SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrPReady);
         mbar_arrive(smem_u32(&bar_p_full[sb]));
 
         if (!more) {
           // ---- epilogue of this item
           const int64_t t = item / p.n_groups;
           const int g = static_cast<int>(item % p.n_groups);
-          const int head = g * kGroupHeads + h;
-          if (row_owner) {
-            const bool empty = !(l_sum > 0.f);
-            float den = l_sum;
-            if (p.attn_sink) den += exp2f(fmaf(__ldg(p.attn_sink + head), kLog2e, -m_used));
-            s_inv[h] = empty ? 0.f : 1.f / den;
-            const int64_t o = t * p.h_q + head;
-            p.lse[o] = empty ? INFINITY : (m_used + log2f(l_sum)) * kLn2;
-            p.max_logits[o] = empty ? -INFINITY : s_max * p.sm_scale;
+          if (quad_leader) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              const int h = x ? hB : hA;
+              const int head = g * kGroupHeads + h;
+              const bool empty = !(l_sum[x] > 0.f);
+              float den = l_sum[x];
+              if (p.attn_sink) den += exp2f(fmaf(__ldg(p.attn_sink + head), kLog2e, -m_used[x]));
+              s_inv[h] = empty ? 0.f : 1.f / den;
+              const int64_t o = t * p.h_q + head;
+              p.lse[o] = empty ? INFINITY : (m_used[x] + log2f(l_sum[x])) * kLn2;
+              p.max_logits[o] = empty ? -INFINITY : s_max[x] * p.sm_scale;
+            }
           }
           wait_or_flag(smem_u32(&bar_o_done[sb]), (b >> 1) & 1, abort, lim);
           named_bar_sync(2, 128);
           tc_fence_after();
-          if (q == 0 && lane == 0) SMLA_TRACE_EVENT(b, kTrEpilogue);
+          SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrEpilogue);
           __nv_bfloat16* out_t = p.out + (t * p.h_q + g * kGroupHeads) * static_cast<int64_t>(kDv);
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
@@ -503,11 +547,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t flags_even = 0u, flags_odd = 0u;  // ring flags of the blocks with QK issued
       bool have_desc = false;
       uint32_t desc_flags = 0u;
+      int qk_ks = 0;                             // k-steps of QK(next_qk) issued so far
+      int64_t q_issued = 0;                      // Q tiles requested so far (one per item)
       uint64_t t_progress = globaltimer_ns();
       uint32_t spins = 0;
       while (pv_items < n_my_items) {
         if (*abort) break;
         bool progressed = false;
+        // Q tile of the next item, once the previous item's last S = QK^T has completed
+        if (q_issued < n_my_items &&
+            (q_issued == 0 ||
+             (q_issued <= qk_items && mbar_test_wait(smem_u32(&bar_q_empty), (q_issued - 1) & 1)))) {
+          const int64_t item = blockIdx.x + q_issued * gridDim.x;
+          const int64_t t = item / p.n_groups;
+          const int g = static_cast<int>(item % p.n_groups);
+          mbar_arrive_expect_tx(smem_u32(&bar_q_full), kTileBytes);
+          const int qrow = static_cast<int>(t * p.h_q + g * kGroupHeads);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, qrow, smem_u32(&bar_q_full));
+          ++q_issued;
+          progressed = true;
+        }
         if (next_pv < next_qk) {
           const int sb = static_cast<int>(next_pv & 1);
           const uint32_t fl = sb ? flags_odd : flags_even;
@@ -535,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             progressed = true;
           }
         }
-        if (!progressed && next_qk <= next_pv + 1 && qk_items < n_my_items) {
+        if (!progressed && next_qk <= next_pv + kQkLead && qk_items < n_my_items) {
           const int r = static_cast<int>(next_qk % kRing);
           if (!have_desc && mbar_test_wait(smem_u32(&bar_ring_full[r]), (next_qk / kRing) & 1)) {
             desc_flags = ring[r].flags;
@@ -545,27 +605,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (have_desc) {
             const int s = static_cast<int>(next_qk & 1);
             const bool first = (desc_flags & kFirstBlock) != 0;
-            bool ok = mbar_test_wait(smem_u32(&bar_kv_full[s]), (next_qk >> 1) & 1);
-            if (ok && first) ok = mbar_test_wait(smem_u32(&bar_q_full), qk_items & 1);
+            bool ok = qk_ks > 0;                 // a started block needs no further checks
+            if (!ok) {
+              ok = mbar_test_wait(smem_u32(&bar_kv_full[s]), (next_qk >> 1) & 1);
+              if (ok && first) ok = mbar_test_wait(smem_u32(&bar_q_full), qk_items & 1);
+              if (ok) {
+                tc_fence_after();
+                SMLA_TRACE_EVENT(next_qk, kTrQkIssue);
+              }
+            }
             if (ok) {
-              tc_fence_after();
-              SMLA_TRACE_EVENT(next_qk, kTrQkIssue);
+              // S = QK^T of the whole block at once: interleaving PV MMAs into an unfinished
+              // accumulation chain stalls the tensor pipe.
               const uint64_t qd0 = make_sdesc_sw128(q_base, 16, 1024);
               const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
+              const int ks_end = min(qk_ks + kQkSlice, kQkSteps);
 #pragma unroll 4
-              for (int ks = 0; ks < kQkSteps; ++ks) {
+              for (int ks = qk_ks; ks < ks_end; ++ks) {
                 const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
                 umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
               }
-              umma_commit(smem_u32(&bar_s_full[s]));
-              if (desc_flags & kLastBlock) {
-                umma_commit(smem_u32(&bar_q_empty));
-                ++qk_items;
+              qk_ks = ks_end;
+              if (qk_ks == kQkSteps) {
+                umma_commit(smem_u32(&bar_s_full[s]));
+                if (desc_flags & kLastBlock) {
+                  umma_commit(smem_u32(&bar_q_empty));
+                  ++qk_items;
+                }
+                if (s) flags_odd = desc_flags;
+                else flags_even = desc_flags;
+                have_desc = false;
+                qk_ks = 0;
+                ++next_qk;
               }
-              if (s) flags_odd = desc_flags;
-              else flags_even = desc_flags;
-              have_desc = false;
-              ++next_qk;
               progressed = true;
             }
           }
@@ -573,14 +645,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (progressed) {
           t_progress = globaltimer_ns();
           spins = 0;
-        } else if ((++spins & 63u) == 0u && globaltimer_ns() - t_progress > lim) {
-          *abort = 1;
-          atomicExch(&g_device_status, static_cast<int>(SMLA_ERR_DEVICE_TIMEOUT));
+        } else {
+          // nothing ready: back off briefly so this poll does not steal issue slots from the
+          // softmax warp that shares its scheduler
+          __nanosleep(32);
+          if ((++spins & 63u) == 0u && globaltimer_ns() - t_progress > lim) {
+            *abort = 1;
+            atomicExch(&g_device_status, static_cast<int>(SMLA_ERR_DEVICE_TIMEOUT));
+          }
         }
       }
-      // drain: every MMA issued above completes before TMEM is released
+      // drain: every MMA issued above completes before TMEM is released, and the last Q tile
+      // requested has landed before the CTA may exit
       umma_commit(smem_u32(&bar_final));
       wait_drain(smem_u32(&bar_final), 0, lim);
+      if (q_issued > 0) wait_drain(smem_u32(&bar_q_full), (q_issued - 1) & 1, lim);
     }
     __syncwarp();
   }
@@ -801,7 +880,7 @@ const char* sparse_mla_status_string(smla_status s) {
 int sparse_mla_abi_version(void) { return SMLA_ABI_VERSION; }
 
 #ifdef SMLA_TRACE
-// Debug builds only: copies the pipeline trace of CTA 0 ([256 blocks][7 events] int64 clock
+// Debug builds only: copies the pipeline trace of CTA 0 ([256 blocks][12 events] int64 clock
 // stamps) into `dst` (host memory).
 int sparse_mla_trace_fetch(long long* dst) {
   return cudaMemcpyFromSymbol(dst, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
