@@ -183,6 +183,34 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(x, device=None):
+    """Max of a float over every rank of the default process group: the job's time is its
+    slowest rank's.  A no-op without an initialised group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, device=None):
+    """Sum of a float over every rank (the units all ranks processed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def job_tflops(total_flops, total_ms):
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return total_flops / (total_ms * 1e-3) / 1e12
+
+
 def run_reference(args, world, rank):
     """fp64 CPU oracle as the reference arm: each step is the oracle on a bounded sample of the
     workload's rows, spread over the batch."""
@@ -330,14 +358,10 @@ def main():
     barrier()
     t1 = time.time()
     clocks = sampler.stop(t0, t1)
-    total_ms = float(np.sum(step_ms))
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(float(np.sum(step_ms)), dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    job_flops = sum_over_ranks(flops, dev)      # every rank runs its own batch of this shape
+    value = job_tflops(job_flops * args.steps, total_ms)
     launches = args.steps
 
     # the same rows with topk_length passed (padding-overhead check), non-paged ramp only
@@ -379,9 +403,10 @@ def main():
             if i >= 2:
                 e_ms.append(a.elapsed_time(b))
         launches_e2e = args.e2e_steps + 2
-        e2e = {"value": world * flops / (float(np.mean(e_ms)) * 1e-3) / 1e12, "unit": UNIT,
+        e2e_ms = max_over_ranks(float(np.mean(e_ms)), dev)
+        e2e = {"value": job_tflops(job_flops, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": float(np.mean(e_ms))}
+               "ms_per_step": e2e_ms}
         launches += launches_e2e
 
     status = smla.sparse_mla_device_status()

@@ -40,22 +40,25 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    P = ctypes.c_void_p
+    I64, I32, D = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    lib.smla_oracle_fwd.restype = ctypes.c_int
+    lib.smla_oracle_fwd.argtypes = [P, P, P, P, P, D, I64, I64, I32, I32, I32, I32, P, I64,
+                                    P, P, P, I32]
+    lib.smla_oracle_fwd_paged.restype = ctypes.c_int
+    lib.smla_oracle_fwd_paged.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, P, D, I64,
+                                          I32, I32, I32, I32, P, I64, P, P, P, I32]
+    lib.smla_oracle_last_valid_length.restype = None
+    lib.smla_oracle_last_valid_length.argtypes = [P, I64, I32, I64, P]
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            I64, I32, D = ctypes.c_int64, ctypes.c_int, ctypes.c_double
-            lib.smla_oracle_fwd.restype = ctypes.c_int
-            lib.smla_oracle_fwd.argtypes = [P, P, P, P, P, D, I64, I64, I32, I32, I32, I32, P, I64,
-                                            P, P, P, I32]
-            lib.smla_oracle_fwd_paged.restype = ctypes.c_int
-            lib.smla_oracle_fwd_paged.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, P, D, I64,
-                                                  I32, I32, I32, I32, P, I64, P, P, P, I32]
-            lib.smla_oracle_last_valid_length.restype = None
-            lib.smla_oracle_last_valid_length.argtypes = [P, I64, I32, I64, P]
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
 
 
@@ -68,12 +71,12 @@ def _c(a, dtype):
 
 
 def sparse_mla_fwd(q_bits, kv_bits, indices, topk_length=None, attn_sink=None, sm_scale=None,
-                   d_v=512, rows=None, threads=0):
+                   d_v=512, rows=None, threads=0, _lib_=None):
     """fp64 reference.  q_bits [s_q, h_q, d_qk] uint16, kv_bits [s_kv, 1, d_qk] (or [s_kv, d_qk])
     uint16, indices [s_q, 1, topk] (or [s_q, topk]) int32.  Returns (O, lse, max_logits) as
     float64 arrays of shape [n, h_q, d_v], [n, h_q], [n, h_q] for the listed rows (all rows when
     ``rows`` is None)."""
-    lib = _load()
+    lib = _lib_ or _load()
     q_bits = _c(q_bits, np.uint16)
     kv_bits = _c(kv_bits, np.uint16)
     indices = _c(indices, np.int32)
@@ -99,9 +102,9 @@ def sparse_mla_fwd(q_bits, kv_bits, indices, topk_length=None, attn_sink=None, s
 
 def sparse_mla_fwd_paged(q_bits, kv_pool_bits, block_table, indices, page_block=64,
                          seqlens_k=None, s_kv_per_req=0, s_q_per_req=1, topk_length=None,
-                         attn_sink=None, sm_scale=None, d_v=512, rows=None, threads=0):
+                         attn_sink=None, sm_scale=None, d_v=512, rows=None, threads=0, _lib_=None):
     """fp64 reference over a paged KV cache; same outputs as :func:`sparse_mla_fwd`."""
-    lib = _load()
+    lib = _lib_ or _load()
     q_bits = _c(q_bits, np.uint16)
     kv_pool_bits = _c(kv_pool_bits, np.uint16)
     block_table = _c(block_table, np.int32)
@@ -129,12 +132,30 @@ def sparse_mla_fwd_paged(q_bits, kv_pool_bits, block_table, indices, page_block=
     return out, lse, mx
 
 
-def last_valid_length(indices, s_kv):
+def last_valid_length(indices, s_kv, _lib_=None):
     """One past the last slot holding 0 <= idx < s_kv in each row (0 for rows without one)."""
-    lib = _load()
+    lib = _lib_ or _load()
     indices = _c(indices, np.int32)
     s_q = indices.shape[0]
     topk = indices.reshape(s_q, -1).shape[1]
     out = np.empty(s_q, np.int32)
     lib.smla_oracle_last_valid_length(_ptr(indices), s_q, topk, int(s_kv), _ptr(out))
     return out
+
+
+class Variant:
+    """The same three calls bound to another build of the oracle source (a shared library at
+    ``path``).  The pin tests use it to check that planted mistakes in the arithmetic are
+    caught; nothing else does."""
+
+    def __init__(self, path):
+        self._lib = _bind(ctypes.CDLL(path))
+
+    def sparse_mla_fwd(self, *a, **kw):
+        return sparse_mla_fwd(*a, _lib_=self._lib, **kw)
+
+    def sparse_mla_fwd_paged(self, *a, **kw):
+        return sparse_mla_fwd_paged(*a, _lib_=self._lib, **kw)
+
+    def last_valid_length(self, *a, **kw):
+        return last_valid_length(*a, _lib_=self._lib, **kw)
