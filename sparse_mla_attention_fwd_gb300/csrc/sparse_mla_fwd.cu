@@ -56,24 +56,24 @@ constexpr int kBlockN = 64;            // keys per k-block
 constexpr int kGroupHeads = 64;        // heads per work item
 constexpr int kDv = 512;               // value width (first d_v columns of each kv row)
 // 12 warps = 3 per SM sub-partition (warp w runs on sub-partition w % 4), so each thread may
-// hold up to 168 registers.  The MMA issuer and the scheduler share sub-partition 2 with one
-// softmax warp and no gather warp, whose TMA issue would compete with UMMA issue.
+// hold up to 168 registers.  S = QK^T and O^T += V^T P^T are issued by two different threads:
+// the tensor unit interleaves two independent issue streams without the dead time a single
+// issuer leaves between chains (it is blocked inside each chain's issue until the chain has
+// nearly drained, then has to find the next ready chain).
 constexpr int kThreads = 384;
-constexpr int kGatherWarps = 6;        // warps 0, 1, 3, 8, 9, 11
+constexpr int kGatherWarps = 5;        // warps 0, 1, 3, 8, 9
 constexpr int kSoftmaxWarp0 = 4;       // warps 4-7 (TMEM lane quadrants 0-3)
-constexpr int kMmaWarp = 2;            // also issues the Q tile loads
+constexpr int kQkWarp = 2;             // QK issuer; also allocates TMEM and loads Q tiles
+constexpr int kPvWarp = 11;            // PV issuer
 constexpr int kSchedWarp = 10;
 constexpr int kRing = 8;               // scheduler ring depth (blocks)
-constexpr int kRingConsumers = kGatherWarps + 4 + 1;   // arrivals that free a ring slot
+constexpr int kRingConsumers = kGatherWarps + 4 + 2;   // arrivals that free a ring slot
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O^T: 4 chunks x 64 columns
 constexpr uint32_t kTmemS = 256;       // S buffers: 256 + 64*b
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleLog2 = 8.0f;
-#ifndef SMLA_QK_LEAD
-#define SMLA_QK_LEAD 1
-#endif   // rescale O only when the running max grows by > 2^8
+constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the running max grows by > 2^8
 
 enum : uint32_t { kFirstBlock = 1u, kLastBlock = 2u };
 
@@ -188,10 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kChunks = D_QK / 64;                 // 128-byte column chunks of a row
   constexpr uint32_t kTileBytes = kChunks * 8192u;   // 64 rows x D_QK bf16 (= Q tile = stage)
   constexpr int kQkSteps = D_QK / 16;
-  constexpr int kQkSlice = kQkSteps;                // QK k-steps issued per polling step
-  // QK(b) may be issued once PV(b - kQkLead) has been.  1 (measured best): S of the next
-  // block is computed while this block's softmax runs; 0 = strict QK(b), PV(b), QK(b+1).
-  constexpr int kQkLead = SMLA_QK_LEAD;
   // P^T (64 heads x 64 keys bf16, 8 KB) of block b lives in the rope chunk (columns 512..575)
   // of stage b%2 when there is one -- that chunk is dead once S = QK^T has been computed --
   // and in a separate double buffer otherwise.
@@ -207,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_ring_full[kRing], bar_ring_empty[kRing];
   __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty;
   __shared__ __align__(8) uint64_t bar_kv_full[2], bar_kv_empty[2];
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2], bar_o_free, bar_final;
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2], bar_o_free;
+  __shared__ __align__(8) uint64_t bar_final_qk, bar_final_pv;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ float s_alpha[kGroupHeads];
@@ -243,10 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bar_o_done[s]), 1);
     }
     mbar_init(smem_u32(&bar_o_free), 128);
-    mbar_init(smem_u32(&bar_final), 1);
+    mbar_init(smem_u32(&bar_final_qk), 1);
+    mbar_init(smem_u32(&bar_final_pv), 1);
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -304,11 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp < kSoftmaxWarp0 && warp != kMmaWarp || warp >= kSoftmaxWarp0 + 4) {
+  } else if (warp < 2 || warp == 3 || warp == 8 || warp == 9) {
     // ======================================================== gather
     // TMA issue throughput grows with the number of issuing warps, so the 16*kChunks gather4
-    // items of a block are dealt round-robin over the 6 gather warps.
-    const int gw = warp < 2 ? warp : (warp == 3 ? 2 : (warp < kSchedWarp ? warp - 5 : 5));   // 0..5
+    // items of a block are dealt round-robin over the 5 gather warps.
+    const int gw = warp < 2 ? warp : (warp == 3 ? 2 : warp - 5);   // 0..4
     const int it = gw + kGatherWarps * lane;                  // item: (4-row group, column chunk)
     const int grp = it & 15;
     const int chunk = it >> 4;
@@ -531,135 +529,102 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ======================================================== MMA issuer
+  } else if (warp == kQkWarp) {
+    // ======================================================== QK issuer (and Q tile loads)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc_bf16(64, kBlockN, false, false);
-      constexpr uint32_t idesc_pv = make_idesc_bf16(128, kGroupHeads, true, false);
-      const uint32_t q_base = smem_u32(sQ);
+      const uint64_t qd0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint32_t kv_base = smem_u32(sKV);
-      // Blocks are issued in order.  S is double buffered, so QK(b) may run at most one block
-      // ahead of PV(b-1).  Both are polled: PV is issued as soon as its P is ready (it frees a
-      // KV stage for the gather warps), QK as soon as its stage has landed.
-      int64_t next_qk = 0, next_pv = 0;
-      int64_t qk_items = 0;                      // items whose last QK has been issued
-      int64_t pv_items = 0;                      // items whose last PV has been issued
-      uint32_t flags_even = 0u, flags_odd = 0u;  // ring flags of the blocks with QK issued
-      bool have_desc = false;
-      uint32_t desc_flags = 0u;
-      int qk_ks = 0;                             // k-steps of QK(next_qk) issued so far
-      int64_t q_issued = 0;                      // Q tiles requested so far (one per item)
-      uint64_t t_progress = globaltimer_ns();
-      uint32_t spins = 0;
-      while (pv_items < n_my_items) {
-        if (*abort) break;
-        bool progressed = false;
-        // Q tile of the next item, once the previous item's last S = QK^T has completed
-        if (q_issued < n_my_items &&
-            (q_issued == 0 ||
-             (q_issued <= qk_items && mbar_test_wait(smem_u32(&bar_q_empty), (q_issued - 1) & 1)))) {
-          const int64_t item = blockIdx.x + q_issued * gridDim.x;
-          const int64_t t = item / p.n_groups;
-          const int g = static_cast<int>(item % p.n_groups);
-          mbar_arrive_expect_tx(smem_u32(&bar_q_full), kTileBytes);
-          const int qrow = static_cast<int>(t * p.h_q + g * kGroupHeads);
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, qrow, smem_u32(&bar_q_full));
-          ++q_issued;
-          progressed = true;
-        }
-        if (next_pv < next_qk) {
-          const int sb = static_cast<int>(next_pv & 1);
-          const uint32_t fl = sb ? flags_odd : flags_even;
-          const bool first = (fl & kFirstBlock) != 0;
-          bool ok = mbar_test_wait(smem_u32(&bar_p_full[sb]), (next_pv >> 1) & 1);
-          if (ok && first && pv_items > 0) ok = mbar_test_wait(smem_u32(&bar_o_free), (pv_items - 1) & 1);
-          if (ok) {
-            tc_fence_after();
-            SMLA_TRACE_EVENT(next_pv, kTrPvIssue);
-            // descriptor start addresses advance in 16-byte units (low 14 bits)
-            const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
-            const uint64_t b0 = make_sdesc_sw128(smem_u32(p_addr(static_cast<int>(next_pv))), 16, 1024);
-#pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
+      auto load_q = [&](int64_t i) {
+        const int64_t item = blockIdx.x + i * gridDim.x;
+        const int64_t t = item / p.n_groups;
+        const int g = static_cast<int>(item % p.n_groups);
+        mbar_arrive_expect_tx(smem_u32(&bar_q_full), kTileBytes);
+        const int qrow = static_cast<int>(t * p.h_q + g * kGroupHeads);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, qrow, smem_u32(&bar_q_full));
+      };
+      int64_t q_loaded = 0;                      // Q tiles requested so far
+      if (n_my_items > 0) {
+        load_q(0);
+        q_loaded = 1;
+      }
+      int64_t b = 0;
+      for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
+        wait_or_flag(smem_u32(&bar_q_full), i & 1, abort, lim);
+        for (bool more = true; more && !*abort; ++b) {
+          const int r = static_cast<int>(b % kRing);
+          const int s = static_cast<int>(b & 1);
+          wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
+          more = (ring[r].flags & kLastBlock) == 0;
+          mbar_arrive(smem_u32(&bar_ring_empty[r]));
+          wait_or_flag(smem_u32(&bar_kv_full[s]), (b >> 1) & 1, abort, lim);
+          // S buffer s was last read by the softmax of block b-2
+          if (b >= 2) wait_or_flag(smem_u32(&bar_p_full[s]), ((b - 2) >> 1) & 1, abort, lim);
+          tc_fence_after();
+          SMLA_TRACE_EVENT(b, kTrQkIssue);
+          const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
 #pragma unroll
-              for (int ks = 0; ks < kBlockN / 16; ++ks) {
-                umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
-                        b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
-              }
-            }
-            umma_commit(smem_u32(&bar_kv_empty[sb]));
-            umma_commit(smem_u32(&bar_o_done[sb]));
-            if (fl & kLastBlock) ++pv_items;
-            ++next_pv;
-            progressed = true;
+          for (int ks = 0; ks < kQkSteps; ++ks) {
+            const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+            umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
           }
+          umma_commit(smem_u32(&bar_s_full[s]));
+          SMLA_TRACE_EVENT(b, kTrSLoaded);
         }
-        if (!progressed && next_qk <= next_pv + kQkLead && qk_items < n_my_items) {
-          const int r = static_cast<int>(next_qk % kRing);
-          if (!have_desc && mbar_test_wait(smem_u32(&bar_ring_full[r]), (next_qk / kRing) & 1)) {
-            desc_flags = ring[r].flags;
-            mbar_arrive(smem_u32(&bar_ring_empty[r]));
-            have_desc = true;
-          }
-          if (have_desc) {
-            const int s = static_cast<int>(next_qk & 1);
-            const bool first = (desc_flags & kFirstBlock) != 0;
-            bool ok = qk_ks > 0;                 // a started block needs no further checks
-            if (!ok) {
-              ok = mbar_test_wait(smem_u32(&bar_kv_full[s]), (next_qk >> 1) & 1);
-              if (ok && first) ok = mbar_test_wait(smem_u32(&bar_q_full), qk_items & 1);
-              if (ok) {
-                tc_fence_after();
-                SMLA_TRACE_EVENT(next_qk, kTrQkIssue);
-              }
-            }
-            if (ok) {
-              // S = QK^T of the whole block at once: interleaving PV MMAs into an unfinished
-              // accumulation chain stalls the tensor pipe.
-              const uint64_t qd0 = make_sdesc_sw128(q_base, 16, 1024);
-              const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
-              const int ks_end = min(qk_ks + kQkSlice, kQkSteps);
-#pragma unroll 4
-              for (int ks = qk_ks; ks < ks_end; ++ks) {
-                const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-                umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
-              }
-              qk_ks = ks_end;
-              if (qk_ks == kQkSteps) {
-                umma_commit(smem_u32(&bar_s_full[s]));
-                if (desc_flags & kLastBlock) {
-                  umma_commit(smem_u32(&bar_q_empty));
-                  ++qk_items;
-                }
-                if (s) flags_odd = desc_flags;
-                else flags_even = desc_flags;
-                have_desc = false;
-                qk_ks = 0;
-                ++next_qk;
-              }
-              progressed = true;
-            }
-          }
-        }
-        if (progressed) {
-          t_progress = globaltimer_ns();
-          spins = 0;
-        } else {
-          // nothing ready: back off briefly so this poll does not steal issue slots from the
-          // softmax warp that shares its scheduler
-          __nanosleep(32);
-          if ((++spins & 63u) == 0u && globaltimer_ns() - t_progress > lim) {
-            *abort = 1;
-            atomicExch(&g_device_status, static_cast<int>(SMLA_ERR_DEVICE_TIMEOUT));
-          }
+        // the next item's Q tile replaces this one once this item's last S = QK^T is done
+        if (i + 1 < n_my_items && !*abort) {
+          umma_commit(smem_u32(&bar_q_empty));
+          wait_or_flag(smem_u32(&bar_q_empty), i & 1, abort, lim);
+          load_q(i + 1);
+          ++q_loaded;
         }
       }
       // drain: every MMA issued above completes before TMEM is released, and the last Q tile
       // requested has landed before the CTA may exit
-      umma_commit(smem_u32(&bar_final));
-      wait_drain(smem_u32(&bar_final), 0, lim);
-      if (q_issued > 0) wait_drain(smem_u32(&bar_q_full), (q_issued - 1) & 1, lim);
+      umma_commit(smem_u32(&bar_final_qk));
+      wait_drain(smem_u32(&bar_final_qk), 0, lim);
+      if (q_loaded > 0) wait_drain(smem_u32(&bar_q_full), (q_loaded - 1) & 1, lim);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ======================================================== PV issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, kGroupHeads, true, false);
+      const uint32_t kv_base = smem_u32(sKV);
+      int64_t b = 0;
+      for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
+        for (bool more = true; more && !*abort; ++b) {
+          const int r = static_cast<int>(b % kRing);
+          const int sb = static_cast<int>(b & 1);
+          wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
+          const uint32_t fl = ring[r].flags;
+          mbar_arrive(smem_u32(&bar_ring_empty[r]));
+          more = (fl & kLastBlock) == 0;
+          const bool first = (fl & kFirstBlock) != 0;
+          wait_or_flag(smem_u32(&bar_p_full[sb]), (b >> 1) & 1, abort, lim);
+          // the epilogue of the previous item has read all of O^T
+          if (first && i > 0) wait_or_flag(smem_u32(&bar_o_free), (i - 1) & 1, abort, lim);
+          tc_fence_after();
+          SMLA_TRACE_EVENT(b, kTrPvIssue);
+          // descriptor start addresses advance in 16-byte units (low 14 bits)
+          const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
+          const uint64_t b0 = make_sdesc_sw128(smem_u32(p_addr(static_cast<int>(b))), 16, 1024);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int ks = 0; ks < kBlockN / 16; ++ks) {
+              umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
+                      b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(smem_u32(&bar_kv_empty[sb]));
+          umma_commit(smem_u32(&bar_o_done[sb]));
+          SMLA_TRACE_EVENT(b, kTrSent);
+        }
+      }
+      umma_commit(smem_u32(&bar_final_pv));
+      wait_drain(smem_u32(&bar_final_pv), 0, lim);
     }
     __syncwarp();
   }
@@ -668,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // commit, which tracks all earlier MMAs), so TMEM can be released.
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
