@@ -192,6 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // of stage b%2 when there is one -- that chunk is dead once S = QK^T has been computed --
   // and in a separate double buffer otherwise.
   constexpr bool kPInStage = (kChunks > 8);
+  // A stage is handed over in kGroups groups of columns: group g holds column chunks 2g and
+  // 2g+1 (the last group also the rope chunk).  PV's M-chunk g reads exactly group g's value
+  // columns, so group g of a stage is refilled as soon as PV M-chunk g of the block before has
+  // completed, and S = QK^T of the new block starts on group 0 while later groups are in flight.
+  constexpr int kGroups = 4;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) BlockDesc ring[kRing];
   __shared__ __align__(8) uint64_t bar_ring_full[kRing], bar_ring_empty[kRing];
   __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty;
-  __shared__ __align__(8) uint64_t bar_kv_full[2], bar_kv_empty[2];
+  __shared__ __align__(8) uint64_t bar_kv_full[2][kGroups], bar_kv_empty[2][kGroups];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2], bar_o_free;
   __shared__ __align__(8) uint64_t bar_final_qk, bar_final_pv;
   __shared__ uint32_t tmem_slot;
@@ -233,8 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bar_q_full), 1);
     mbar_init(smem_u32(&bar_q_empty), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bar_kv_full[s]), 1);
-      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+      for (int g = 0; g < kGroups; ++g) {
+        mbar_init(smem_u32(&bar_kv_full[s][g]), 1);
+        mbar_init(smem_u32(&bar_kv_empty[s][g]), 1);
+      }
       mbar_init(smem_u32(&bar_s_full[s]), 1);
       mbar_init(smem_u32(&bar_p_full[s]), 128);
       mbar_init(smem_u32(&bar_o_done[s]), 1);
@@ -304,13 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 2 || warp == 3 || warp == 8 || warp == 9) {
     // ======================================================== gather
-    // TMA issue throughput grows with the number of issuing warps, so the 16*kChunks gather4
-    // items of a block are dealt round-robin over the 5 gather warps.
+    // TMA issue throughput grows with the number of issuing warps, so the 16 x (chunks of a
+    // group) gather4 items of each column group are dealt round-robin over the 5 gather warps.
     const int gw = warp < 2 ? warp : (warp == 3 ? 2 : warp - 5);   // 0..4
-    const int it = gw + kGatherWarps * lane;                  // item: (4-row group, column chunk)
+    const int it = gw + kGatherWarps * lane;        // item within a group: (4-row group, chunk)
     const int grp = it & 15;
-    const int chunk = it >> 4;
-    const int pi = tid;
+    const bool leader = (gw == 0 && lane == 0);
     int64_t b = 0;
     for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
       for (bool more = true; more && !*abort; ++b) {
@@ -318,24 +324,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = static_cast<int>(b & 1);
         wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
         more = (ring[r].flags & kLastBlock) == 0;
-        if (b >= 2) wait_or_flag(smem_u32(&bar_kv_empty[s]), ((b >> 1) - 1) & 1, abort, lim);
-        if (pi == 0) {
-          SMLA_TRACE_EVENT(b, kTrGatherIssue);
-          mbar_arrive_expect_tx(smem_u32(&bar_kv_full[s]), kTileBytes);
-        }
-        if (chunk < kChunks) {
-          const int4 rr = *reinterpret_cast<const int4*>(&ring[r].rows[4 * grp]);
-          tma_gather4(smem_u32(sKV + s * kTileBytes + chunk * 8192 + grp * 512), &kv_map, 64 * chunk,
-                      rr.x, rr.y, rr.z, rr.w, smem_u32(&bar_kv_full[s]));
-        }
+        const int4 rr = *reinterpret_cast<const int4*>(&ring[r].rows[4 * grp]);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_ring_empty[r]));
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+          const int c0 = 2 * g;
+          const int nch = (g == kGroups - 1) ? kChunks - c0 : 2;
+          if (b >= 2) wait_or_flag(smem_u32(&bar_kv_empty[s][g]), ((b >> 1) - 1) & 1, abort, lim);
+          if (leader) {
+            if (g == 0) SMLA_TRACE_EVENT(b, kTrGatherIssue);
+            mbar_arrive_expect_tx(smem_u32(&bar_kv_full[s][g]), nch * 8192u);
+          }
+          if (it < 16 * nch) {
+            const int chunk = c0 + (it >> 4);
+            tma_gather4(smem_u32(sKV + s * kTileBytes + chunk * 8192 + grp * 512), &kv_map, 64 * chunk,
+                        rr.x, rr.y, rr.z, rr.w, smem_u32(&bar_kv_full[s][g]));
+          }
+        }
       }
     }
     // drain: the last fills of both stages have landed before this CTA may exit
-    if (pi == 0) {
+    if (leader) {
       for (int64_t bb = (b >= 2 ? b - 2 : 0); bb < b; ++bb)
-        wait_drain(smem_u32(&bar_kv_full[bb & 1]), (bb >> 1) & 1, lim);
+        for (int g = 0; g < kGroups; ++g)
+          wait_drain(smem_u32(&bar_kv_full[bb & 1][g]), (bb >> 1) & 1, lim);
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
     // ======================================================== softmax / correction / epilogue
@@ -504,6 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(2, 128);
           tc_fence_after();
           SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrEpilogue);
+          // O goes out with direct 2-byte stores: the 32 lanes of a warp hold 32 consecutive d
+          // of one head, 64 contiguous bytes.  (Staging through shared memory for TMA tensor
+          // stores measured slower: the stores queue behind the gathers in the TMA unit.)
           __nv_bfloat16* out_t = p.out + (t * p.h_q + g * kGroupHeads) * static_cast<int64_t>(kDv);
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
@@ -558,16 +574,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
           more = (ring[r].flags & kLastBlock) == 0;
           mbar_arrive(smem_u32(&bar_ring_empty[r]));
-          wait_or_flag(smem_u32(&bar_kv_full[s]), (b >> 1) & 1, abort, lim);
           // S buffer s was last read by the softmax of block b-2
           if (b >= 2) wait_or_flag(smem_u32(&bar_p_full[s]), ((b - 2) >> 1) & 1, abort, lim);
-          tc_fence_after();
-          SMLA_TRACE_EVENT(b, kTrQkIssue);
           const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
+          // S = QK^T group by group, as the column groups of the stage land
 #pragma unroll
-          for (int ks = 0; ks < kQkSteps; ++ks) {
-            const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-            umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
+          for (int g = 0; g < kGroups; ++g) {
+            wait_or_flag(smem_u32(&bar_kv_full[s][g]), (b >> 1) & 1, abort, lim);
+            tc_fence_after();
+            if (g == 0) SMLA_TRACE_EVENT(b, kTrQkIssue);
+            const int ks_end = (g == kGroups - 1) ? kQkSteps : 8 * (g + 1);
+#pragma unroll
+            for (int ks = 8 * g; ks < ks_end; ++ks) {
+              const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+              umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
+            }
           }
           umma_commit(smem_u32(&bar_s_full[s]));
           SMLA_TRACE_EVENT(b, kTrSLoaded);
@@ -617,8 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
                       b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
             }
+            // column group m of this stage has been read by every MMA that needs it (the last
+            // group's commit also covers P^T in the rope chunk)
+            umma_commit(smem_u32(&bar_kv_empty[sb][m]));
           }
-          umma_commit(smem_u32(&bar_kv_empty[sb]));
           umma_commit(smem_u32(&bar_o_done[sb]));
           SMLA_TRACE_EVENT(b, kTrSent);
         }
@@ -752,6 +775,7 @@ smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices
   // an empty KV still needs a one-row map; every slot is then invalid and never read
   if (!make_map(&kvm, kv_base, s_kv > 0 ? static_cast<uint64_t>(s_kv) : 1u, d_qk, 1))
     return SMLA_ERR_TENSOR_MAP;
+
   FwdParams p{};
   p.indices = indices;
   p.topk_length = topk_length;
@@ -795,6 +819,7 @@ smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t poo
   CUtensorMap qm, kvm;
   if (!make_map(&qm, q, static_cast<uint64_t>(s_q) * h_q, d_qk, 64)) return SMLA_ERR_TENSOR_MAP;
   if (!make_map(&kvm, kv_pool, static_cast<uint64_t>(pool_rows), d_qk, 1)) return SMLA_ERR_TENSOR_MAP;
+
   FwdParams p{};
   p.indices = indices;
   p.topk_length = topk_length;
