@@ -2,34 +2,35 @@
 //
 // Each query token t attends to its own list of top-k slots into one shared latent KV
 // (h_kv = 1; K = kv[:, :d_qk], V = kv[:, :d_v]).  A slot j counts iff j < L_t and
-// 0 <= idx[t][j] < s_kv, where L_t is the row's effective length: the caller's topk_length[t]
-// clamped to [0, topk], or, when no topk_length is given, one past the last valid slot found
-// by a tail scan (FlashMLA PR #196, "Fix").  Rows with no valid slot return O = 0,
-// lse = +inf, max_logits = -inf (FlashMLA PR #196, "Correctness notes").  The optional
-// per-head attention sink is a value-less virtual key in the softmax denominator (FlashMLA
-// PR #198, "Summary" item 2).
+// 0 <= idx[t][j] < s_kv, where L_t is the caller's topk_length[t] clamped to [0, topk], or topk
+// when no topk_length is given.  Rows with no counted slot return O = 0, lse = +inf,
+// max_logits = -inf (FlashMLA PR #196, "Correctness notes").  The optional per-head attention
+// sink is a value-less virtual key in the softmax denominator (FlashMLA PR #198, "Summary"
+// item 2).
 //
 // Work item = (token, group of 64 heads).  The kernel is persistent: one CTA per SM walks a
 // static round-robin list of items, and every role streams through the same sequence of
-// 64-key blocks, so one item's tail overlaps the next item's head.
+// 64-key blocks, so one item's tail overlaps the next item's head.  A row's counted slots are
+// packed into dense blocks, so it costs max(ceil(n_counted / 64), 1) blocks: trailing padding
+// costs nothing (the fix of FlashMLA PR #196, "Fix") and neither do invalid entries inside the
+// row.
 //
 // Warp roles (384 threads, 12 warps = 3 per SM sub-partition, warp w on sub-partition w % 4):
-//   warps 0,1,3,8,9,11  gather    : TMA gather4 of the selected KV rows (whole rows: measured
-//                                   ~45% faster per byte than half rows) into a 2-stage ring.
-//                                   The 16 x (d_qk/64) gather4 ops of a block are dealt over
-//                                   the six warps (TMA issue rate grows with issuing warps).
-//                                   A slot that is invalid or past L_t carries row coordinate
-//                                   -1, so TMA zero-fills it and its index is never an address.
+//   warps 0,1,3,8,9     gather    : TMA gather4 of the selected KV rows (whole rows: measured
+//                                   ~45% faster per byte than half rows) into a 2-stage ring,
+//                                   each stage handed over in four column groups.  A slot
+//                                   without a counted index carries row coordinate -1, so TMA
+//                                   zero-fills it and its index is never an address.
 //   warps 4-7           softmax   : online exp2 softmax on S read as 16x256b TMEM fragments
 //                                   (every lane holds 2 heads x 16 keys), P -> smem, lazy O
 //                                   rescale, epilogue (sink, normalise, write O / lse / max).
-//   warp 2              MMA       : TMEM allocation, Q tile loads, tcgen05.mma issue (one
-//                                   thread polling every readiness barrier without blocking).
-//   warp 10             scheduler : per item, derives L_t (topk_length or tail scan) and the
-//                                   block count max(ceil(L_t/64), 1); per block, resolves the 64
-//                                   slots to row coordinates and a validity mask in a shared
-//                                   ring.  It runs ahead, so index loads never sit on the
-//                                   critical path, and every role reads the same block count.
+//   warp 2              QK issuer : TMEM allocation, Q tile loads, S = QK^T.
+//   warp 11             PV issuer : O^T += V^T P^T.
+//   warp 10             scheduler : per row, one pass over its index list that packs the
+//                                   counted slots into 64-slot blocks (resolved TMA row
+//                                   coordinates + validity mask + first/last flags) in a shared
+//                                   8-deep ring.  It runs ahead, so index loads never sit on the
+//                                   critical path.
 // Tensor-core work per 64-key block:
 //   S[64 heads x 64 keys]  = Q_g . K_blk^T        (M=64, N=64, K=d_qk; both K-major SW128)
 //   O^T[512 x 64 heads]   += V_blk^T . P^T        (4 x M=128, N=64, K=64; V^T read MN-major
@@ -262,52 +263,140 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kSchedWarp) {
     // ======================================================== scheduler
+    // Per row, a parallel scan first finds the last counted slot (j < L_t, 0 <= idx < s_kv) and
+    // the number of counted slots.  A row whose counted slots form a dense prefix (the usual
+    // case: front-packed lists, -1 or INT_MAX padding) is cut into blocks straight from its
+    // slot list, so trailing padding costs nothing (FlashMLA PR #196, "Fix").  Any other row is
+    // packed: its counted slots go, in slot order, into dense blocks, so invalid entries inside
+    // the row cost nothing either.  The result does not depend on the packing (it is invariant
+    // under permuting slots and inserting invalid ones; the oracle's pins check both).  A row
+    // costs max(ceil(n_counted / 64), 1) blocks, and every role walks the same block stream.
+    const uint32_t lanes_below = (1u << lane) - 1u;
+    auto acquire = [&](int64_t blk) {
+      if (blk >= kRing)
+        wait_or_flag(smem_u32(&bar_ring_empty[blk % kRing]), ((blk / kRing) - 1) & 1, abort, lim);
+    };
+    auto publish = [&](int64_t blk, uint32_t m0, uint32_t m1, uint32_t flags, int64_t item) {
+      const int r = static_cast<int>(blk % kRing);
+      if (lane == 0) {
+        ring[r].mask[0] = m0;
+        ring[r].mask[1] = m1;
+        ring[r].item = static_cast<int32_t>(item);
+        ring[r].flags = flags;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        SMLA_TRACE_EVENT(blk, kTrRing);
+        mbar_arrive(smem_u32(&bar_ring_full[r]));
+      }
+    };
     int64_t b = 0;
     for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
       const int64_t item = blockIdx.x + i * gridDim.x;
       const int64_t t = item / p.n_groups;
       const int32_t* idx_row = p.indices + t * static_cast<int64_t>(p.topk);
       const int64_t kv_len = row_kv_len<PAGED>(p, t);
-      int L;
-      if (DYNAMIC) {
-        L = min(max(__ldg(p.topk_length + t), 0), p.topk);
-      } else {
-        // tail scan: one past the last slot that holds a valid index (FlashMLA PR #196, "Fix")
-        int last = -1;
-        for (int j = lane; j < p.topk; j += 32)
-          if (slot_ok<PAGED>(p, __ldg(idx_row + j), kv_len)) last = j;
+      const int Lr = DYNAMIC ? min(max(__ldg(p.topk_length + t), 0), p.topk) : p.topk;
+      int last = -1, cnt = 0;
+      if constexpr (PAGED) {
+        // Decode-shaped work has few blocks per CTA, so the scan's load latency is exposed:
+        // pull the next row's list into L2 and keep eight 32-slot chunks of loads in flight.
+        // (On the prefill paths, which are throughput-bound, this form measured slower.)
+        if (i + 1 < n_my_items) {
+          const int64_t tn = (item + gridDim.x) / p.n_groups;
+          const char* nrow = reinterpret_cast<const char*>(p.indices + tn * static_cast<int64_t>(p.topk));
+          for (int off = lane * 128; off < p.topk * 4; off += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + off));
+        }
+        for (int j0 = 0; j0 < Lr; j0 += 8 * 32) {
+          int vals[8];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-        L = last + 1;
-      }
-      const int nblk = max((L + kBlockN - 1) / kBlockN, 1);
-      for (int k = 0; k < nblk && !*abort; ++k, ++b) {
-        const int r = static_cast<int>(b % kRing);
-        if (b >= kRing) wait_or_flag(smem_u32(&bar_ring_empty[r]), ((b / kRing) - 1) & 1, abort, lim);
-        uint32_t m[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int slot = k * kBlockN + 32 * h + lane;
-          int coord = -1;
-          if (slot < L) {
-            const int v = __ldg(idx_row + slot);
-            if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + 32 * u + lane;
+            vals[u] = j < Lr ? __ldg(idx_row + j) : -1;
           }
-          ring[r].rows[32 * h + lane] = coord;
-          m[h] = __ballot_sync(0xffffffffu, slot < L && coord >= 0);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + 32 * u + lane;
+            if (j < Lr && slot_ok<PAGED>(p, vals[u], kv_len)) {
+              last = j;
+              ++cnt;
+            }
+          }
         }
-        if (lane == 0) {
-          ring[r].mask[0] = m[0];
-          ring[r].mask[1] = m[1];
-          ring[r].item = static_cast<int32_t>(item);
-          ring[r].flags = (k == 0 ? kFirstBlock : 0u) | (k == nblk - 1 ? kLastBlock : 0u);
-        }
-        __syncwarp();
-        if (lane == 0) {
-          SMLA_TRACE_EVENT(b, kTrRing);
-          mbar_arrive(smem_u32(&bar_ring_full[r]));
-        }
+      } else {
+        for (int j = lane; j < Lr; j += 32)
+          if (slot_ok<PAGED>(p, __ldg(idx_row + j), kv_len)) {
+            last = j;
+            ++cnt;
+          }
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      }
+      const int L = last + 1;
+      if (cnt == L) {
+        // dense prefix: block k holds slots 64k .. 64k+63 of the list
+        const int nblk = max((L + kBlockN - 1) / kBlockN, 1);
+        for (int k = 0; k < nblk && !*abort; ++k, ++b) {
+          const int r = static_cast<int>(b % kRing);
+          acquire(b);
+          uint32_t m[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int slot = k * kBlockN + 32 * h + lane;
+            int coord = -1;
+            if (slot < L) {
+              const int v = __ldg(idx_row + slot);
+              if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+            }
+            ring[r].rows[32 * h + lane] = coord;
+            m[h] = __ballot_sync(0xffffffffu, coord >= 0);
+          }
+          publish(b, m[0], m[1], (k == 0 ? kFirstBlock : 0u) | (k == nblk - 1 ? kLastBlock : 0u), item);
+        }
+        continue;
+      }
+      // packing pass over [0, L): the indices were just read and come from L1
+      const int64_t b0 = b;
+      int count = 0;               // counted slots packed so far
+      int64_t acquired = b0 - 1;   // last block whose ring slot is held
+      int64_t published = b0;      // next block to publish
+      for (int j0 = 0; j0 < L && !*abort; j0 += 32) {
+        const int slot = j0 + lane;
+        int coord = -1;
+        if (slot < L) {
+          const int v = __ldg(idx_row + slot);
+          if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, coord >= 0);
+        if (bal == 0u) continue;
+        const int n = __popc(bal);
+        const int64_t newest = b0 + (count + n - 1) / kBlockN;   // block of the newest slot
+        while (acquired < newest) acquire(++acquired);
+        if (coord >= 0) {
+          const int pos = count + __popc(bal & lanes_below);
+          ring[(b0 + pos / kBlockN) % kRing].rows[pos % kBlockN] = coord;
+        }
+        count += n;
+        __syncwarp();
+        // every block before the newest one is full and has a successor
+        for (; published < newest; ++published)
+          publish(published, 0xffffffffu, 0xffffffffu, published == b0 ? kFirstBlock : 0u, item);
+      }
+      // the block that holds the row's last counted slot (or one empty block) closes the item
+      if (count == 0) acquire(++acquired);
+      const int64_t lastb = b0 + (count > 0 ? (count - 1) / kBlockN : 0);
+      const int fill = count - static_cast<int>(lastb - b0) * kBlockN;   // 0..64 slots used
+      const int rl = static_cast<int>(lastb % kRing);
+      for (int e = fill + lane; e < kBlockN; e += 32) ring[rl].rows[e] = -1;
+      const uint32_t m0 = fill >= 32 ? 0xffffffffu : ((1u << fill) - 1u);
+      const uint32_t m1 = fill >= 64 ? 0xffffffffu : (fill > 32 ? ((1u << (fill - 32)) - 1u) : 0u);
+      __syncwarp();
+      publish(lastb, m0, m1, (lastb == b0 ? kFirstBlock : 0u) | kLastBlock, item);
+      b = lastb + 1;
     }
   } else if (warp < 2 || warp == 3 || warp == 8 || warp == 9) {
     // ======================================================== gather

@@ -185,3 +185,46 @@ def test_decode_fixed_equals_dynamic():
 def test_no_device_timeouts_recorded():
     import sparse_mla_attention_fwd_gb300 as smla
     assert smla.sparse_mla_device_status() == 0
+
+
+# ---------------------------------------------------------------- block packing
+def _scattered_row_case(seed, s_q=12, s_kv=900, h_q=64, d_qk=576, topk=640):
+    """Rows whose counted slots are spread among invalid entries (-1, >= s_kv, INT_MAX, other
+    negatives), with counts on and around block boundaries, and the same rows front-packed."""
+    rng = np.random.default_rng(seed)
+    q = W.normal_bf16(rng, (s_q, h_q, d_qk))
+    kv = W.normal_bf16(rng, (s_kv, 1, d_qk))
+    counts = [0, 1, 63, 64, 65, 127, 128, 129, 200, 333, 511, 640][:s_q]
+    spread = np.full((s_q, topk), -1, np.int32)
+    packed = np.full((s_q, topk), -1, np.int32)
+    bad = np.array([-1, s_kv, s_kv + 7, W.INT_MAX, -9], np.int32)
+    for i, n in enumerate(counts):
+        vals = rng.choice(s_kv, size=n, replace=False).astype(np.int32)
+        pos = np.sort(rng.choice(topk, size=n, replace=False))
+        if i == 4:
+            pos = np.arange(topk - n, topk)          # counted slots only at the far end
+        row = rng.choice(bad, size=topk)
+        row[pos] = vals
+        spread[i] = row
+        packed[i, :n] = vals
+    base = dict(q=q, kv=kv, topk_length=None, attn_sink=rng.standard_normal(h_q).astype(np.float32),
+                sm_scale=float(np.float32(1 / np.sqrt(d_qk))), d_v=512, paged=False)
+    return (dict(base, indices=spread.reshape(s_q, 1, topk)), dict(base, indices=packed.reshape(s_q, 1, topk)))
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_packed_blocks_match_oracle(seed):
+    spread, _ = _scattered_row_case(seed)
+    assert_parity(to_np(run_gpu(spread)), run_oracle(spread), f"scattered rows seed {seed}")
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_invalid_entries_do_not_change_a_bit(seed):
+    # Counted slots are packed in slot order into dense blocks, so a row with invalid entries
+    # anywhere computes exactly the same blocks, in the same order, as the row with them
+    # removed: outputs must agree bit for bit (FlashMLA PR #196, "Correctness notes": invalid
+    # entries are masked wherever they sit).
+    spread, packed = _scattered_row_case(seed)
+    a, b = run_gpu(spread), run_gpu(packed)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
