@@ -228,3 +228,37 @@ def test_invalid_entries_do_not_change_a_bit(seed):
     a, b = run_gpu(spread), run_gpu(packed)
     assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+# ---------------------------------------------------------------- wider shapes and paged variants
+@pytest.mark.parametrize("h_q,d_qk,topk", [(256, 512, 3000), (192, 576, 700), (1024, 512, 96)])
+def test_many_head_groups_and_long_lists(h_q, d_qk, topk):
+    # several 64-head groups per token (items of one token on different CTAs), lists far
+    # longer than one block, and the largest supported head count
+    w = W.random_case(21 + h_q, 5, 4096, h_q, d_qk, topk, with_sink=True, dup=True)
+    assert_parity(to_np(run_gpu(w)), run_oracle(w), f"h_q={h_q} d_qk={d_qk} topk={topk}")
+
+
+def _paged_case(seed, n_req=6, s_q_per_req=3, page=32, max_blocks=12, h_q=128, d_qk=576, topk=300,
+                with_len=True):
+    rng = np.random.default_rng(seed)
+    n_pages = n_req * max_blocks + 5
+    pool = W.normal_bf16(rng, (n_pages * page, 1, d_qk))
+    q = W.normal_bf16(rng, (n_req * s_q_per_req, h_q, d_qk))
+    bt = rng.permutation(n_pages)[: n_req * max_blocks].astype(np.int32).reshape(n_req, max_blocks)
+    seqlens = rng.integers(0, max_blocks * page + 1, size=n_req).astype(np.int32)
+    seqlens[0] = 0                                   # a request with an empty cache
+    s_q = n_req * s_q_per_req
+    idx = rng.integers(-3, max_blocks * page + 40, size=(s_q, 1, topk)).astype(np.int32)
+    tl = rng.integers(0, topk + 1, size=s_q).astype(np.int32) if with_len else None
+    return dict(q=q, kv=pool, indices=idx, topk_length=tl, attn_sink=rng.standard_normal(h_q).astype(np.float32),
+                sm_scale=float(np.float32(1 / np.sqrt(d_qk))), d_v=512, paged=True, block_table=bt,
+                page_block=page, s_kv_per_req=max_blocks * page, s_q_per_req=s_q_per_req, seqlens_k=seqlens)
+
+
+@pytest.mark.parametrize("with_len", [True, False])
+def test_paged_per_request_lengths(with_len):
+    # per-request cache lengths (seqlens_k), several queries per request, positions beyond a
+    # request's length or its block table, and a request with an empty cache
+    w = _paged_case(31, with_len=with_len)
+    assert_parity(to_np(run_gpu(w)), run_oracle(w), f"paged seqlens len={with_len}")
