@@ -47,7 +47,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["ramp", "full", "scattered", "decode", "tiny"], default="ramp")
+    ap.add_argument("--config", choices=["ramp", "full", "scattered", "decode", "decode_b2", "decode_b8", "tiny"],
+                    default="ramp")
+    ap.add_argument("--n-split", default="auto",
+                    help="split-KV ranges per row: 'auto' (split only when items < SMs) or an integer")
     ap.add_argument("--with-len", action="store_true", help="pass topk_length in the timed steps")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--skip-cpu", action="store_true", help="no CPU-oracle baseline leg")
@@ -65,6 +68,10 @@ def make_workload(name, with_len):
         return W.scattered()
     if name == "decode":
         return W.decode(dynamic=True)
+    if name == "decode_b2":
+        return W.decode_fixed(n_req=2)
+    if name == "decode_b8":
+        return W.decode_fixed(n_req=8)
     return W.tiny(with_len=with_len, with_sink=True)
 
 
@@ -80,6 +87,10 @@ def describe(w, name):
                      f"d_v=512 topk={topk} p_invalid=0.3",
         "decode": f"paged decode B={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} d_v=512 topk={topk} "
                   f"topk_length=1024 INT_MAX suffix, 64-token pages",
+        "decode_b2": f"small-batch paged decode B=2 x S_q=2 s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} d_v=512 "
+                     f"topk={topk} all valid, 64-token pages",
+        "decode_b8": f"small-batch paged decode B=8 x S_q=2 s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} d_v=512 "
+                     f"topk={topk} all valid, 64-token pages",
         "tiny": f"tiny s_q={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} topk={topk}",
     }[name]
     return text
@@ -321,6 +332,10 @@ def main():
     mx = torch.empty((s_q, h_q), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    topk = w["indices"].reshape(s_q, -1).shape[1]
+    n_split = smla.auto_splits(s_q, h_q, topk, dev) if args.n_split == "auto" else int(args.n_split)
+    launches_per_call = 2 if n_split > 1 else 1   # split-KV adds the merge kernel
+
     def call(d, tl="auto"):
         t = d["topk_length"] if isinstance(tl, str) else tl
         if w.get("paged"):
@@ -328,9 +343,10 @@ def main():
                                              page_block=w["page_block"], s_kv_per_req=w["s_kv_per_req"],
                                              s_q_per_req=w["s_q_per_req"], topk_length=t,
                                              attn_sink=d["attn_sink"], sm_scale=w["sm_scale"],
-                                             d_v=w["d_v"], out=out, lse=lse, max_logits=mx, stream=stream)
+                                             d_v=w["d_v"], out=out, lse=lse, max_logits=mx, stream=stream,
+                                             n_split=n_split)
         return smla.sparse_mla_fwd(d["q"], d["kv"], d["indices"], t, d["attn_sink"], sm_scale=w["sm_scale"],
-                                   d_v=w["d_v"], out=out, lse=lse, max_logits=mx, stream=stream)
+                                   d_v=w["d_v"], out=out, lse=lse, max_logits=mx, stream=stream, n_split=n_split)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
 
@@ -362,14 +378,14 @@ def main():
     ms_per_step = total_ms / args.steps
     job_flops = sum_over_ranks(flops, dev)      # every rank runs its own batch of this shape
     value = job_tflops(job_flops * args.steps, total_ms)
-    launches = args.steps
+    launches = args.steps * launches_per_call
 
     # the same rows with topk_length passed (padding-overhead check), non-paged ramp only
     extra = {}
     if args.config == "ramp":
         counts = torch.from_numpy(w["valid_counts"]).to(dev)
         other = timed_steps(max(20, args.steps // 3), tl=(None if args.with_len else counts))
-        launches += len(other)
+        launches += len(other) * launches_per_call
         ms_other = float(np.mean(other))
         ms_no_len, ms_len = (ms_other, ms_per_step) if args.with_len else (ms_per_step, ms_other)
         extra = {"ms_no_topk_length": ms_no_len, "ms_topk_length_passed": ms_len,
@@ -407,7 +423,7 @@ def main():
         e2e = {"value": job_tflops(job_flops, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms}
-        launches += launches_e2e
+        launches += launches_e2e * launches_per_call
 
     status = smla.sparse_mla_device_status()
     if rank != 0:
@@ -430,12 +446,12 @@ def main():
         "data": "synthetic",
         "config": {"workload": describe(w, args.config),
                    "topk_length": "passed" if (args.with_len or w["topk_length"] is not None) else "omitted",
-                   "l2": "flushed (256 MB write) between timed iterations",
+                   "l2": "flushed (256 MB write) between timed iterations", "n_split": n_split,
                    "pct_of_bf16_peak": 100.0 * achieved / peak,
                    "vs_baseline_ref": "FlashMLA PR #196 B200 number (other hardware, context)" if base else None},
         "roofline": roof,
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_call,
         "gpu_launches_total": launches,
         "device_status": status,
     }

@@ -31,13 +31,14 @@
 #ifndef SPARSE_MLA_GB300_H_
 #define SPARSE_MLA_GB300_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 1
+#define SMLA_ABI_VERSION 2
 
 typedef struct CUstream_st* smla_stream_t; /* a cudaStream_t; NULL = legacy default stream */
 
@@ -48,7 +49,8 @@ typedef enum {
   SMLA_ERR_MISALIGNED = 3,     /* a pointer violates the alignment rule above */
   SMLA_ERR_LAUNCH = 4,         /* the CUDA launch (or a CUDA query) failed */
   SMLA_ERR_DEVICE_TIMEOUT = 5, /* a device-side wait gave up (see sparse_mla_device_status) */
-  SMLA_ERR_TENSOR_MAP = 6      /* the TMA descriptor for an operand could not be encoded */
+  SMLA_ERR_TENSOR_MAP = 6,     /* the TMA descriptor for an operand could not be encoded */
+  SMLA_ERR_WORKSPACE = 7       /* split-KV workspace missing or smaller than required */
 } smla_status;
 
 /*
@@ -64,7 +66,9 @@ typedef enum {
  *   max_logits   [s_q, h_q]        fp32   (written)
  * When topk_length is NULL, each row's work is bounded by its last valid slot, found by a
  * scan in the kernel prologue (FlashMLA PR #196, "Fix"); results are identical to passing
- * that length explicitly.
+ * that length explicitly.  A row's counted slots are packed into dense 64-slot blocks, so
+ * invalid entries anywhere in the row cost no compute; the result does not depend on where
+ * they sit.
  */
 smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices,
                            const int32_t* topk_length, const float* attn_sink, float sm_scale,
@@ -92,6 +96,41 @@ smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t poo
                                  const float* attn_sink, float sm_scale, int d_v, void* out,
                                  float* lse, float* max_logits, int64_t s_q, int h_q, int d_qk,
                                  int topk, smla_stream_t stream);
+
+/*
+ * Split-KV variants, for calls with fewer (row, 64-head group) items than SMs (small-batch
+ * decode).  Each row's slot list [0, L_t) is cut into n_split contiguous ranges of
+ * ceil(ceil(L_t / n_split) / 64) * 64 slots; every (row, head group, range) is one work unit
+ * whose partial result (unnormalised O, exponent offset, sum, max) goes to `workspace`, and a
+ * second kernel on the same stream merges a row's ranges with log-sum-exp weights (the sink
+ * joins the denominator there) and writes out / lse / max_logits.  Same semantics and
+ * outputs as sparse_mla_fwd / sparse_mla_fwd_paged up to summation order; with n_split == 1
+ * they are the same call (no workspace needed).
+ *   n_split          1 .. 64
+ *   workspace        device buffer of at least sparse_mla_splitkv_workspace_size(s_q, h_q,
+ *                    n_split) bytes, 256-byte aligned, owned by the caller; its contents
+ *                    need no initialisation and are meaningless after the call.  Two calls
+ *                    in flight at once must not share a workspace.
+ * Errors as in the base calls, plus SMLA_ERR_BAD_SHAPE for n_split outside 1..64 and
+ * SMLA_ERR_WORKSPACE when the workspace is NULL or too small (n_split > 1).
+ */
+size_t sparse_mla_splitkv_workspace_size(int64_t s_q, int h_q, int n_split);
+
+smla_status sparse_mla_fwd_splitkv(const void* q, const void* kv, const int32_t* indices,
+                                   const int32_t* topk_length, const float* attn_sink, float sm_scale,
+                                   int d_v, void* out, float* lse, float* max_logits, int64_t s_q,
+                                   int64_t s_kv, int h_q, int d_qk, int topk, int n_split,
+                                   void* workspace, size_t workspace_bytes, smla_stream_t stream);
+
+smla_status sparse_mla_fwd_paged_splitkv(const void* q, const void* kv_pool, int64_t pool_rows,
+                                         const int32_t* block_table, int max_blocks, int page_block,
+                                         const int32_t* seqlens_k, int64_t s_kv_per_req,
+                                         int s_q_per_req, const int32_t* indices,
+                                         const int32_t* topk_length, const float* attn_sink,
+                                         float sm_scale, int d_v, void* out, float* lse,
+                                         float* max_logits, int64_t s_q, int h_q, int d_qk, int topk,
+                                         int n_split, void* workspace, size_t workspace_bytes,
+                                         smla_stream_t stream);
 
 /*
  * Reads (and, when reset != 0, clears) the device-side status word that kernels set when one

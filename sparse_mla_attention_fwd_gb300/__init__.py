@@ -21,7 +21,7 @@ import torch
 from ._native import EXPORTED, SmlaError, load_library, status_string
 from .native_build import LIB_PATH, build as build_library
 
-__all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_device_status",
+__all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "auto_splits", "sparse_mla_device_status",
            "sparse_mla_status_string", "SmlaError", "load_library", "build_library", "LIB_PATH"]
 
 
@@ -67,11 +67,32 @@ def _outputs(q, h_q, d_v, out, lse, max_logits):
     return out, lse, max_logits
 
 
+def auto_splits(s_q, h_q, topk, device=None):
+    """Split-KV factor for a call: 1 when the (row, 64-head group) items already fill more than
+    half the SMs, else as many ranges per row as keep every (item, range) unit in one wave (at
+    least one 64-slot block per range, at most 64 ranges)."""
+    items = s_q * (h_q // 64)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    if items == 0 or 2 * items > sms:
+        return 1
+    # one wave of (item, range) units, each range at least one 64-slot block
+    return int(max(1, min(64, sms // items, -(-topk // 64))))
+
+
+def _workspace(lib, s_q, h_q, n_split, device):
+    n = int(lib.sparse_mla_splitkv_workspace_size(int(s_q), int(h_q), int(n_split)))
+    if n == 0:
+        return None, 0
+    return torch.empty(n, dtype=torch.uint8, device=device), n
+
+
 def sparse_mla_fwd(q, kv, indices, topk_length=None, attn_sink=None, sm_scale=None, d_v=512,
-                   out=None, lse=None, max_logits=None, stream=None):
+                   out=None, lse=None, max_logits=None, stream=None, n_split=1):
     """q [s_q, h_q, d_qk] bf16; kv [s_kv, 1, d_qk] (or [s_kv, d_qk]) bf16; indices [s_q, 1, topk]
     (or [s_q, topk]) int32; topk_length [s_q] int32 or None; attn_sink [h_q] fp32 or None.
-    Returns (out [s_q, h_q, d_v] bf16, lse [s_q, h_q] fp32, max_logits [s_q, h_q] fp32)."""
+    Returns (out [s_q, h_q, d_v] bf16, lse [s_q, h_q] fp32, max_logits [s_q, h_q] fp32).
+    n_split > 1 (or "auto": see auto_splits) runs the split-KV variant with a workspace
+    allocated here."""
     lib = load_library()
     _check(q, "q", torch.bfloat16)
     dev = q.device
@@ -93,11 +114,21 @@ def sparse_mla_fwd(q, kv, indices, topk_length=None, attn_sink=None, sm_scale=No
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d_qk)
     out, lse, max_logits = _outputs(q, h_q, d_v, out, lse, max_logits)
+    if n_split == "auto":
+        n_split = auto_splits(s_q, h_q, topk, dev)
     with torch.cuda.device(dev):
-        rc = lib.sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length), _ptr(attn_sink),
-                                float(sm_scale), int(d_v), _ptr(out), _ptr(lse), _ptr(max_logits),
-                                int(s_q), int(s_kv), int(h_q), int(d_qk), int(topk),
-                                _stream_handle(stream, dev))
+        if n_split == 1:
+            rc = lib.sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length), _ptr(attn_sink),
+                                    float(sm_scale), int(d_v), _ptr(out), _ptr(lse), _ptr(max_logits),
+                                    int(s_q), int(s_kv), int(h_q), int(d_qk), int(topk),
+                                    _stream_handle(stream, dev))
+        else:
+            ws, nbytes = _workspace(lib, s_q, h_q, n_split, dev)
+            rc = lib.sparse_mla_fwd_splitkv(_ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length),
+                                            _ptr(attn_sink), float(sm_scale), int(d_v), _ptr(out), _ptr(lse),
+                                            _ptr(max_logits), int(s_q), int(s_kv), int(h_q), int(d_qk),
+                                            int(topk), int(n_split), _ptr(ws), int(nbytes),
+                                            _stream_handle(stream, dev))
     if rc != 0:
         raise SmlaError(rc, "sparse_mla_fwd")
     return out, lse, max_logits
@@ -105,7 +136,8 @@ def sparse_mla_fwd(q, kv, indices, topk_length=None, attn_sink=None, sm_scale=No
 
 def sparse_mla_fwd_paged(q, kv_pool, block_table, indices, page_block=64, seqlens_k=None,
                          s_kv_per_req=None, s_q_per_req=1, topk_length=None, attn_sink=None,
-                         sm_scale=None, d_v=512, out=None, lse=None, max_logits=None, stream=None):
+                         sm_scale=None, d_v=512, out=None, lse=None, max_logits=None, stream=None,
+                         n_split=1):
     """Paged-KV variant: kv_pool [n_pages*page_block, 1, d_qk] bf16, block_table [n_req,
     max_blocks] int32, seqlens_k [n_req] int32 or None (then every request has s_kv_per_req
     tokens); indices hold token positions within the row's request."""
@@ -133,13 +165,23 @@ def sparse_mla_fwd_paged(q, kv_pool, block_table, indices, page_block=64, seqlen
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d_qk)
     out, lse, max_logits = _outputs(q, h_q, d_v, out, lse, max_logits)
+    if n_split == "auto":
+        n_split = auto_splits(s_q, h_q, topk, dev)
     with torch.cuda.device(dev):
-        rc = lib.sparse_mla_fwd_paged(_ptr(q), _ptr(kv_pool), int(pool_rows), _ptr(block_table),
-                                      int(max_blocks), int(page_block), _ptr(seqlens_k),
-                                      int(s_kv_per_req), int(s_q_per_req), _ptr(indices),
-                                      _ptr(topk_length), _ptr(attn_sink), float(sm_scale), int(d_v),
-                                      _ptr(out), _ptr(lse), _ptr(max_logits), int(s_q), int(h_q),
-                                      int(d_qk), int(topk), _stream_handle(stream, dev))
+        if n_split == 1:
+            rc = lib.sparse_mla_fwd_paged(_ptr(q), _ptr(kv_pool), int(pool_rows), _ptr(block_table),
+                                          int(max_blocks), int(page_block), _ptr(seqlens_k),
+                                          int(s_kv_per_req), int(s_q_per_req), _ptr(indices),
+                                          _ptr(topk_length), _ptr(attn_sink), float(sm_scale), int(d_v),
+                                          _ptr(out), _ptr(lse), _ptr(max_logits), int(s_q), int(h_q),
+                                          int(d_qk), int(topk), _stream_handle(stream, dev))
+        else:
+            ws, nbytes = _workspace(lib, s_q, h_q, n_split, dev)
+            rc = lib.sparse_mla_fwd_paged_splitkv(
+                _ptr(q), _ptr(kv_pool), int(pool_rows), _ptr(block_table), int(max_blocks), int(page_block),
+                _ptr(seqlens_k), int(s_kv_per_req), int(s_q_per_req), _ptr(indices), _ptr(topk_length),
+                _ptr(attn_sink), float(sm_scale), int(d_v), _ptr(out), _ptr(lse), _ptr(max_logits), int(s_q),
+                int(h_q), int(d_qk), int(topk), int(n_split), _ptr(ws), int(nbytes), _stream_handle(stream, dev))
     if rc != 0:
         raise SmlaError(rc, "sparse_mla_fwd_paged")
     return out, lse, max_logits

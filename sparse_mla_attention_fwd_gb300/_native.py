@@ -14,8 +14,9 @@ from .native_build import LIB_PATH
 SMLA_OK = 0
 STATUS_NAMES = {0: "SMLA_OK", 1: "SMLA_ERR_NULL_PTR", 2: "SMLA_ERR_BAD_SHAPE",
                 3: "SMLA_ERR_MISALIGNED", 4: "SMLA_ERR_LAUNCH", 5: "SMLA_ERR_DEVICE_TIMEOUT",
-                6: "SMLA_ERR_TENSOR_MAP"}
-EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_device_status",
+                6: "SMLA_ERR_TENSOR_MAP", 7: "SMLA_ERR_WORKSPACE"}
+EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_splitkv_workspace_size",
+            "sparse_mla_fwd_splitkv", "sparse_mla_fwd_paged_splitkv", "sparse_mla_device_status",
             "sparse_mla_status_string", "sparse_mla_abi_version")
 
 _lock = threading.Lock()
@@ -46,6 +47,15 @@ def load_library(path: str | None = None):
         lib.sparse_mla_fwd_paged.restype = I32
         lib.sparse_mla_fwd_paged.argtypes = [P, P, I64, P, I32, I32, P, I64, I32, P, P, P, F32, I32,
                                              P, P, P, I64, I32, I32, I32, P]
+        SZ = ctypes.c_size_t
+        lib.sparse_mla_splitkv_workspace_size.restype = SZ
+        lib.sparse_mla_splitkv_workspace_size.argtypes = [I64, I32, I32]
+        lib.sparse_mla_fwd_splitkv.restype = I32
+        lib.sparse_mla_fwd_splitkv.argtypes = [P, P, P, P, P, F32, I32, P, P, P, I64, I64, I32, I32, I32,
+                                               I32, P, SZ, P]
+        lib.sparse_mla_fwd_paged_splitkv.restype = I32
+        lib.sparse_mla_fwd_paged_splitkv.argtypes = [P, P, I64, P, I32, I32, P, I64, I32, P, P, P, F32, I32,
+                                                     P, P, P, I64, I32, I32, I32, I32, P, SZ, P]
         lib.sparse_mla_device_status.restype = I32
         lib.sparse_mla_device_status.argtypes = [I32]
         lib.sparse_mla_status_string.restype = ctypes.c_char_p

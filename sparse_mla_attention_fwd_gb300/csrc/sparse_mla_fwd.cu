@@ -123,6 +123,12 @@ struct FwdParams {
   int s_q_per_req;
   int64_t pool_rows;           // rows the KV tensor map covers
   uint64_t wait_limit_ns;
+  // split-KV: each item's slot list is cut into n_split ranges, one work unit each, whose
+  // partial results go to part_o [unit][64 heads][512] (unnormalised O) and part_stats
+  // [unit][3][64] (exponent offset m in log2 units, sum l, max of sm_scale * q.k)
+  int n_split;
+  float* part_o;
+  float* part_stats;
 };
 
 // One 64-key block as resolved by the scheduler warp.
@@ -182,7 +188,9 @@ __device__ __forceinline__ int kv_row_of(const FwdParams& p, int64_t t, int v) {
   return (page < 0 || row >= p.pool_rows) ? -1 : static_cast<int>(row);
 }
 
-template <int D_QK, bool DYNAMIC, bool PAGED>
+// SPLIT: work units are (item, slot range); the epilogue writes the unit's partial result to
+// the split-KV workspace instead of O / lse / max_logits (a second kernel merges the ranges).
+template <int D_QK, bool DYNAMIC, bool PAGED, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_fwd_kernel(const __grid_constant__ CUtensorMap q_map,
                           const __grid_constant__ CUtensorMap kv_map, const FwdParams p) {
@@ -221,9 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   volatile int* abort = &abort_flag;
   const uint64_t lim = p.wait_limit_ns;
-  // items of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
-  const int64_t n_my_items =
-      p.n_items > blockIdx.x ? (p.n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  // work units of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...  A unit is an item
+  // (token, 64-head group) or, with SPLIT, an (item, slot range) pair.
+  const int64_t n_units = SPLIT ? p.n_items * p.n_split : p.n_items;
+  const int64_t n_my_items = n_units > blockIdx.x ? (n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto item_of_unit = [&](int64_t u) -> int64_t { return SPLIT ? u / p.n_split : u; };
 
   auto p_addr = [&](int b) -> uint8_t* {
     if constexpr (kPInStage) return sKV + (b & 1) * kTileBytes + 8 * 8192;
@@ -292,18 +302,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int64_t b = 0;
     for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-      const int64_t item = blockIdx.x + i * gridDim.x;
-      const int64_t t = item / p.n_groups;
+      const int64_t unit = blockIdx.x + i * gridDim.x;
+      const int64_t item = unit;   // what the ring carries: the unit (the item itself unless SPLIT)
+      const int64_t t = item_of_unit(unit) / p.n_groups;
       const int32_t* idx_row = p.indices + t * static_cast<int64_t>(p.topk);
       const int64_t kv_len = row_kv_len<PAGED>(p, t);
-      const int Lr = DYNAMIC ? min(max(__ldg(p.topk_length + t), 0), p.topk) : p.topk;
+      int Lr = DYNAMIC ? min(max(__ldg(p.topk_length + t), 0), p.topk) : p.topk;
+      if constexpr (SPLIT) {
+        // this unit's share of the row: range `split` of n_split 64-aligned ranges of [0, L_t)
+        const int split = static_cast<int>(unit % p.n_split);
+        const int span = ((Lr + p.n_split - 1) / p.n_split + kBlockN - 1) / kBlockN * kBlockN;
+        const int j0 = min(split * span, Lr);
+        idx_row += j0;
+        Lr = min(Lr - j0, span);
+      }
       int last = -1, cnt = 0;
       if constexpr (PAGED) {
         // Decode-shaped work has few blocks per CTA, so the scan's load latency is exposed:
         // pull the next row's list into L2 and keep eight 32-slot chunks of loads in flight.
         // (On the prefill paths, which are throughput-bound, this form measured slower.)
         if (i + 1 < n_my_items) {
-          const int64_t tn = (item + gridDim.x) / p.n_groups;
+          const int64_t tn = item_of_unit(unit + gridDim.x) / p.n_groups;
           const char* nrow = reinterpret_cast<const char*>(p.indices + tn * static_cast<int64_t>(p.topk));
           for (int off = lane * 128; off < p.topk * 4; off += 32 * 128)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + off));
@@ -585,10 +604,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(smem_u32(&bar_p_full[sb]));
 
         if (!more) {
-          // ---- epilogue of this item
-          const int64_t t = item / p.n_groups;
-          const int g = static_cast<int>(item % p.n_groups);
-          if (quad_leader) {
+          // ---- epilogue of this item (or, with SPLIT, of this unit)
+          const int64_t unit = item;
+          const int64_t it_ = item_of_unit(unit);
+          const int64_t t = it_ / p.n_groups;
+          const int g = static_cast<int>(it_ % p.n_groups);
+          if constexpr (SPLIT) {
+            // partial result: exponent offset, sum and max per head; unnormalised O^T below
+            if (quad_leader) {
+              float* st = p.part_stats + unit * (3 * kGroupHeads);
+#pragma unroll
+              for (int x = 0; x < 2; ++x) {
+                const int h = x ? hB : hA;
+                const bool empty = !(l_sum[x] > 0.f);
+                st[h] = empty ? -INFINITY : m_used[x];
+                st[kGroupHeads + h] = empty ? 0.f : l_sum[x];
+                st[2 * kGroupHeads + h] = empty ? -INFINITY : s_max[x] * p.sm_scale;
+              }
+            }
+          } else if (quad_leader) {
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
               const int h = x ? hB : hA;
@@ -606,13 +640,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(2, 128);
           tc_fence_after();
           SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrEpilogue);
-          // O goes out with direct 2-byte stores: the 32 lanes of a warp hold 32 consecutive d
-          // of one head, 64 contiguous bytes.  (Staging through shared memory for TMA tensor
-          // stores measured slower: the stores queue behind the gathers in the TMA unit.)
+          // O goes out with direct stores: the 32 lanes of a warp hold 32 consecutive d of one
+          // head (64 contiguous bytes of bf16, or 128 of fp32 partials).  (Staging through
+          // shared memory for TMA tensor stores measured slower: the stores queue behind the
+          // gathers in the TMA unit.)
           __nv_bfloat16* out_t = p.out + (t * p.h_q + g * kGroupHeads) * static_cast<int64_t>(kDv);
+          float* part_t = SPLIT ? p.part_o + unit * (kGroupHeads * kDv) : nullptr;
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
-            __nv_bfloat16* dst = out_t + 128 * m + 32 * q + lane;   // column d of head 0
+            const int dcol = 128 * m + 32 * q + lane;   // column d of this lane
 #pragma unroll 1
             for (int i4 = 0; i4 < 4; ++i4) {
               uint32_t rg[16];
@@ -623,11 +659,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(smem_u32(&bar_o_free));
               }
+              if constexpr (SPLIT) {
 #pragma unroll
-              for (int jj = 0; jj < 16; ++jj) {
-                const float inv = s_inv[16 * i4 + jj];
-                const float val = (inv == 0.f) ? 0.f : __uint_as_float(rg[jj]) * inv;
-                dst[(16 * i4 + jj) * kDv] = __float2bfloat16_rn(val);
+                for (int jj = 0; jj < 16; ++jj) part_t[(16 * i4 + jj) * kDv + dcol] = __uint_as_float(rg[jj]);
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                  const float inv = s_inv[16 * i4 + jj];
+                  const float val = (inv == 0.f) ? 0.f : __uint_as_float(rg[jj]) * inv;
+                  out_t[(16 * i4 + jj) * kDv + dcol] = __float2bfloat16_rn(val);
+                }
               }
             }
           }
@@ -641,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qd0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint32_t kv_base = smem_u32(sKV);
       auto load_q = [&](int64_t i) {
-        const int64_t item = blockIdx.x + i * gridDim.x;
+        const int64_t item = item_of_unit(blockIdx.x + i * gridDim.x);
         const int64_t t = item / p.n_groups;
         const int g = static_cast<int>(item % p.n_groups);
         mbar_arrive_expect_tx(smem_u32(&bar_q_full), kTileBytes);
@@ -751,6 +792,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------------ split-KV merge
+// One CTA per item (token, 64-head group): the n_split partial results of its slot ranges are
+// merged with the standard log-sum-exp weights.  With M = max_s m_s (log2 units),
+//   L = sum_s 2^(m_s - M) l_s,   O = sum_s 2^(m_s - M) O_s / (L + [sink] 2^(sink log2e - M)),
+//   lse = (M + log2 L) ln 2 (sink excluded),   max_logits = max_s max_s,
+// and a head without any counted slot gets O = 0, lse = +inf, max_logits = -inf.  With one
+// range this is the same arithmetic as the single-pass epilogue.
+constexpr int kMaxSplit = 64;
+constexpr int kMergeHeads = 1;       // heads per merge CTA (many small CTAs: loads in flight)
+constexpr int kMergeThreads = 128;   // four value columns d per thread (float4)
+
+__global__ void __launch_bounds__(kMergeThreads)
+    splitkv_merge_kernel(const FwdParams p) {
+  // grid: (item, group of kMergeHeads heads)
+  __shared__ float w[kMergeHeads][kMaxSplit];
+  __shared__ float sst[3][kMaxSplit][kMergeHeads];   // m, l, max of this CTA's heads per range
+  __shared__ float inv[kMergeHeads];
+  const int64_t item = blockIdx.x;
+  const int h0 = blockIdx.y * kMergeHeads;
+  const int64_t t = item / p.n_groups;
+  const int g = static_cast<int>(item % p.n_groups);
+  const int tid = threadIdx.x;
+  const int ns = p.n_split;
+  const float* st0 = p.part_stats + item * ns * (3 * kGroupHeads);
+  // every statistic of every range in one parallel pass (their load latencies overlap)
+  for (int e = tid; e < 3 * ns * kMergeHeads; e += kMergeThreads) {
+    const int k = e / (ns * kMergeHeads), r = e % (ns * kMergeHeads);
+    const int s2 = r / kMergeHeads, hh = r % kMergeHeads;
+    sst[k][s2][hh] = st0[s2 * (3 * kGroupHeads) + k * kGroupHeads + h0 + hh];
+  }
+  __syncthreads();
+  if (tid < kMergeHeads) {
+    const int h = h0 + tid;
+    float M = -INFINITY, mx = -INFINITY;
+    for (int s2 = 0; s2 < ns; ++s2) {
+      M = fmaxf(M, sst[0][s2][tid]);
+      mx = fmaxf(mx, sst[2][s2][tid]);
+    }
+    float L = 0.f;
+    for (int s2 = 0; s2 < ns; ++s2) {
+      const float ms = sst[0][s2][tid];
+      const float ws = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      w[tid][s2] = ws;
+      L = fmaf(ws, sst[1][s2][tid], L);
+    }
+    const int head = g * kGroupHeads + h;
+    const bool empty = !(L > 0.f);
+    float den = L;
+    if (p.attn_sink && !empty) den += exp2f(fmaf(__ldg(p.attn_sink + head), kLog2e, -M));
+    inv[tid] = empty ? 0.f : 1.f / den;
+    const int64_t o = t * p.h_q + head;
+    p.lse[o] = empty ? INFINITY : (M + log2f(L)) * kLn2;
+    p.max_logits[o] = empty ? -INFINITY : mx;
+  }
+  __syncthreads();
+  const float* po = p.part_o + item * ns * static_cast<int64_t>(kGroupHeads * kDv);
+  __nv_bfloat16* out_t = p.out + (t * p.h_q + g * kGroupHeads) * static_cast<int64_t>(kDv);
+#pragma unroll
+  for (int hh = 0; hh < kMergeHeads; ++hh) {
+    const int h = h0 + hh;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s2 = 0; s2 < ns; ++s2) {
+      const float ws = w[hh][s2];
+      const float4 v = __ldg(reinterpret_cast<const float4*>(po + (s2 * kGroupHeads + h) * static_cast<int64_t>(kDv)) + tid);
+      acc.x = fmaf(ws, v.x, acc.x);
+      acc.y = fmaf(ws, v.y, acc.y);
+      acc.z = fmaf(ws, v.z, acc.z);
+      acc.w = fmaf(ws, v.w, acc.w);
+    }
+    const float iv = inv[hh];
+    __nv_bfloat162 lo = __floats2bfloat162_rn(iv == 0.f ? 0.f : acc.x * iv, iv == 0.f ? 0.f : acc.y * iv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(iv == 0.f ? 0.f : acc.z * iv, iv == 0.f ? 0.f : acc.w * iv);
+    // two 4-byte stores: out is only required to be 4-byte aligned
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out_t + h * kDv + 4 * tid);
+    dst[0] = *reinterpret_cast<uint32_t*>(&lo);
+    dst[1] = *reinterpret_cast<uint32_t*>(&hi);
+  }
+}
+
 // ------------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -788,10 +909,10 @@ int sm_count() {
   return n;
 }
 
-template <int D_QK, bool DYNAMIC, bool PAGED>
+template <int D_QK, bool DYNAMIC, bool PAGED, bool SPLIT>
 smla_status launch_one(const CUtensorMap& qm, const CUtensorMap& kvm, const FwdParams& p,
                        cudaStream_t stream) {
-  auto kern = sparse_mla_fwd_kernel<D_QK, DYNAMIC, PAGED>;
+  auto kern = sparse_mla_fwd_kernel<D_QK, DYNAMIC, PAGED, SPLIT>;
   constexpr int kChunks = D_QK / 64;
   const size_t smem = 3 * kChunks * 8192 + (kChunks > 8 ? 0 : 2 * 8192) + 1024;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -799,11 +920,18 @@ smla_status launch_one(const CUtensorMap& qm, const CUtensorMap& kvm, const FwdP
     return SMLA_ERR_LAUNCH;
   const int sms = sm_count();
   if (sms <= 0) return SMLA_ERR_LAUNCH;
-  // persistent: one CTA per SM (the shared-memory footprint admits only one), items assigned
-  // round-robin
-  const int64_t grid = p.n_items < sms ? p.n_items : sms;
+  // persistent: one CTA per SM (the shared-memory footprint admits only one), work units
+  // assigned round-robin
+  const int64_t units = SPLIT ? p.n_items * p.n_split : p.n_items;
+  const int64_t grid = units < sms ? units : sms;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(qm, kvm, p);
-  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
+  if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_LAUNCH;
+  if constexpr (SPLIT) {
+    splitkv_merge_kernel<<<dim3(static_cast<unsigned>(p.n_items), kGroupHeads / kMergeHeads), kMergeThreads, 0,
+                           stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_LAUNCH;
+  }
+  return SMLA_OK;
 }
 
 template <bool PAGED>
@@ -811,11 +939,19 @@ smla_status dispatch(int d_qk, bool dynamic, const CUtensorMap& qm, const CUtens
                      const FwdParams& p, cudaStream_t stream) {
   // topk_length presence is a compile-time choice (FlashMLA PR #216, "Why template<bool
   // DYNAMIC_TOPK>"): the fixed path carries no length load or tail predicate.
-  if (d_qk == 512)
-    return dynamic ? launch_one<512, true, PAGED>(qm, kvm, p, stream)
-                   : launch_one<512, false, PAGED>(qm, kvm, p, stream);
-  return dynamic ? launch_one<576, true, PAGED>(qm, kvm, p, stream)
-                 : launch_one<576, false, PAGED>(qm, kvm, p, stream);
+  const bool split = p.n_split > 1;
+  if (d_qk == 512) {
+    if (split)
+      return dynamic ? launch_one<512, true, PAGED, true>(qm, kvm, p, stream)
+                     : launch_one<512, false, PAGED, true>(qm, kvm, p, stream);
+    return dynamic ? launch_one<512, true, PAGED, false>(qm, kvm, p, stream)
+                   : launch_one<512, false, PAGED, false>(qm, kvm, p, stream);
+  }
+  if (split)
+    return dynamic ? launch_one<576, true, PAGED, true>(qm, kvm, p, stream)
+                   : launch_one<576, false, PAGED, true>(qm, kvm, p, stream);
+  return dynamic ? launch_one<576, true, PAGED, false>(qm, kvm, p, stream)
+                 : launch_one<576, false, PAGED, false>(qm, kvm, p, stream);
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
@@ -843,19 +979,48 @@ constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 }  // namespace
 }  // namespace smla
 
-using namespace smla;
 
-extern "C" {
+namespace smla {
+namespace {
 
-smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices,
-                           const int32_t* topk_length, const float* attn_sink, float sm_scale,
-                           int d_v, void* out, float* lse, float* max_logits, int64_t s_q,
-                           int64_t s_kv, int h_q, int d_qk, int topk, cudaStream_t stream) {
+// Bytes of split-KV workspace for s_q rows x (h_q / 64) groups x n_split ranges: the partial
+// O block of every unit, then its statistics (256-byte aligned).
+size_t splitkv_bytes(int64_t s_q, int h_q, int n_split, size_t* stats_offset) {
+  const int64_t units = s_q * (h_q / kGroupHeads) * n_split;
+  const size_t o_bytes = static_cast<size_t>(units) * kGroupHeads * kDv * sizeof(float);
+  const size_t off = (o_bytes + 255) & ~static_cast<size_t>(255);
+  if (stats_offset) *stats_offset = off;
+  return off + static_cast<size_t>(units) * 3 * kGroupHeads * sizeof(float);
+}
+
+// Validates the split-KV arguments and points p at the workspace.  n_split == 1 needs none.
+smla_status set_split(FwdParams& p, int64_t s_q, int h_q, int n_split, void* workspace,
+                      size_t workspace_bytes) {
+  if (n_split < 1 || n_split > kMaxSplit) return SMLA_ERR_BAD_SHAPE;
+  if (s_q * (h_q / kGroupHeads) * static_cast<int64_t>(n_split) > INT32_MAX) return SMLA_ERR_BAD_SHAPE;
+  p.n_split = n_split;
+  if (n_split == 1) return SMLA_OK;
+  if (!workspace) return SMLA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SMLA_ERR_MISALIGNED;
+  size_t stats_off = 0;
+  if (workspace_bytes < splitkv_bytes(s_q, h_q, n_split, &stats_off)) return SMLA_ERR_WORKSPACE;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_stats = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + stats_off);
+  return SMLA_OK;
+}
+
+smla_status fwd_flat(const void* q, const void* kv, const int32_t* indices, const int32_t* topk_length,
+                     const float* attn_sink, float sm_scale, int d_v, void* out, float* lse,
+                     float* max_logits, int64_t s_q, int64_t s_kv, int h_q, int d_qk, int topk,
+                     int n_split, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (s_kv < 0 || s_kv > INT32_MAX) return SMLA_ERR_BAD_SHAPE;
   // with an empty KV every slot is invalid and kv is never read: it may then be NULL
   const void* kv_base = s_kv > 0 ? kv : q;
   smla_status st = check_common(q, kv_base, indices, out, lse, max_logits, s_q, h_q, d_qk, d_v,
                                 topk, sm_scale);
+  if (st != SMLA_OK) return st;
+  FwdParams p{};
+  st = set_split(p, s_q, h_q, n_split, workspace, workspace_bytes);
   if (st != SMLA_OK || s_q == 0) return st;
   if (attn_sink && !aligned4(attn_sink)) return SMLA_ERR_MISALIGNED;
   if (topk_length && !aligned4(topk_length)) return SMLA_ERR_MISALIGNED;
@@ -864,8 +1029,6 @@ smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices
   // an empty KV still needs a one-row map; every slot is then invalid and never read
   if (!make_map(&kvm, kv_base, s_kv > 0 ? static_cast<uint64_t>(s_kv) : 1u, d_qk, 1))
     return SMLA_ERR_TENSOR_MAP;
-
-  FwdParams p{};
   p.indices = indices;
   p.topk_length = topk_length;
   p.attn_sink = attn_sink;
@@ -887,15 +1050,17 @@ smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices
   return dispatch<false>(d_qk, topk_length != nullptr, qm, kvm, p, stream);
 }
 
-smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t pool_rows,
-                                 const int32_t* block_table, int max_blocks, int page_block,
-                                 const int32_t* seqlens_k, int64_t s_kv_per_req, int s_q_per_req,
-                                 const int32_t* indices, const int32_t* topk_length,
-                                 const float* attn_sink, float sm_scale, int d_v, void* out,
-                                 float* lse, float* max_logits, int64_t s_q, int h_q, int d_qk,
-                                 int topk, cudaStream_t stream) {
+smla_status fwd_paged(const void* q, const void* kv_pool, int64_t pool_rows, const int32_t* block_table,
+                      int max_blocks, int page_block, const int32_t* seqlens_k, int64_t s_kv_per_req,
+                      int s_q_per_req, const int32_t* indices, const int32_t* topk_length,
+                      const float* attn_sink, float sm_scale, int d_v, void* out, float* lse,
+                      float* max_logits, int64_t s_q, int h_q, int d_qk, int topk, int n_split,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   smla_status st = check_common(q, kv_pool, indices, out, lse, max_logits, s_q, h_q, d_qk, d_v,
                                 topk, sm_scale);
+  if (st != SMLA_OK) return st;
+  FwdParams p{};
+  st = set_split(p, s_q, h_q, n_split, workspace, workspace_bytes);
   if (st != SMLA_OK || s_q == 0) return st;
   if (pool_rows < 1 || pool_rows > INT32_MAX || max_blocks < 1 || page_block < 1 ||
       s_q_per_req < 1 || s_kv_per_req < 0 || s_kv_per_req > INT32_MAX ||
@@ -908,8 +1073,6 @@ smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t poo
   CUtensorMap qm, kvm;
   if (!make_map(&qm, q, static_cast<uint64_t>(s_q) * h_q, d_qk, 64)) return SMLA_ERR_TENSOR_MAP;
   if (!make_map(&kvm, kv_pool, static_cast<uint64_t>(pool_rows), d_qk, 1)) return SMLA_ERR_TENSOR_MAP;
-
-  FwdParams p{};
   p.indices = indices;
   p.topk_length = topk_length;
   p.attn_sink = attn_sink;
@@ -933,6 +1096,62 @@ smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t poo
   return dispatch<true>(d_qk, topk_length != nullptr, qm, kvm, p, stream);
 }
 
+}  // namespace
+}  // namespace smla
+
+using namespace smla;
+
+extern "C" {
+
+smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices,
+                           const int32_t* topk_length, const float* attn_sink, float sm_scale,
+                           int d_v, void* out, float* lse, float* max_logits, int64_t s_q,
+                           int64_t s_kv, int h_q, int d_qk, int topk, cudaStream_t stream) {
+  return fwd_flat(q, kv, indices, topk_length, attn_sink, sm_scale, d_v, out, lse, max_logits, s_q,
+                  s_kv, h_q, d_qk, topk, 1, nullptr, 0, stream);
+}
+
+smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t pool_rows,
+                                 const int32_t* block_table, int max_blocks, int page_block,
+                                 const int32_t* seqlens_k, int64_t s_kv_per_req, int s_q_per_req,
+                                 const int32_t* indices, const int32_t* topk_length,
+                                 const float* attn_sink, float sm_scale, int d_v, void* out,
+                                 float* lse, float* max_logits, int64_t s_q, int h_q, int d_qk,
+                                 int topk, cudaStream_t stream) {
+  return fwd_paged(q, kv_pool, pool_rows, block_table, max_blocks, page_block, seqlens_k, s_kv_per_req,
+                   s_q_per_req, indices, topk_length, attn_sink, sm_scale, d_v, out, lse, max_logits,
+                   s_q, h_q, d_qk, topk, 1, nullptr, 0, stream);
+}
+
+size_t sparse_mla_splitkv_workspace_size(int64_t s_q, int h_q, int n_split) {
+  if (s_q < 0 || h_q <= 0 || h_q % kGroupHeads != 0 || n_split < 1 || n_split > kMaxSplit) return 0;
+  if (n_split == 1) return 0;
+  return splitkv_bytes(s_q, h_q, n_split, nullptr);
+}
+
+smla_status sparse_mla_fwd_splitkv(const void* q, const void* kv, const int32_t* indices,
+                                   const int32_t* topk_length, const float* attn_sink, float sm_scale,
+                                   int d_v, void* out, float* lse, float* max_logits, int64_t s_q,
+                                   int64_t s_kv, int h_q, int d_qk, int topk, int n_split,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return fwd_flat(q, kv, indices, topk_length, attn_sink, sm_scale, d_v, out, lse, max_logits, s_q,
+                  s_kv, h_q, d_qk, topk, n_split, workspace, workspace_bytes, stream);
+}
+
+smla_status sparse_mla_fwd_paged_splitkv(const void* q, const void* kv_pool, int64_t pool_rows,
+                                         const int32_t* block_table, int max_blocks, int page_block,
+                                         const int32_t* seqlens_k, int64_t s_kv_per_req,
+                                         int s_q_per_req, const int32_t* indices,
+                                         const int32_t* topk_length, const float* attn_sink,
+                                         float sm_scale, int d_v, void* out, float* lse,
+                                         float* max_logits, int64_t s_q, int h_q, int d_qk, int topk,
+                                         int n_split, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+  return fwd_paged(q, kv_pool, pool_rows, block_table, max_blocks, page_block, seqlens_k, s_kv_per_req,
+                   s_q_per_req, indices, topk_length, attn_sink, sm_scale, d_v, out, lse, max_logits,
+                   s_q, h_q, d_qk, topk, n_split, workspace, workspace_bytes, stream);
+}
+
 smla_status sparse_mla_device_status(int reset) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return SMLA_ERR_LAUNCH;
@@ -952,6 +1171,7 @@ const char* sparse_mla_status_string(smla_status s) {
     case SMLA_ERR_LAUNCH: return "kernel launch failed";
     case SMLA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
     case SMLA_ERR_TENSOR_MAP: return "TMA descriptor encoding failed";
+    case SMLA_ERR_WORKSPACE: return "split-KV workspace missing or too small";
   }
   return "unknown status";
 }

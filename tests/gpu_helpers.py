@@ -26,8 +26,9 @@ def dev_tensor(a, device="cuda:0"):
     return t.to(device)
 
 
-def run_gpu(w, topk_length="auto", indices=None):
-    """Run the workload dict `w` through the CUDA path.  topk_length="auto" uses w's."""
+def run_gpu(w, topk_length="auto", indices=None, n_split=1):
+    """Run the workload dict `w` through the CUDA path.  topk_length="auto" uses w's; n_split > 1
+    runs the split-KV variant."""
     tl = w["topk_length"] if isinstance(topk_length, str) else topk_length
     idx = w["indices"] if indices is None else indices
     if w.get("paged"):
@@ -35,11 +36,11 @@ def run_gpu(w, topk_length="auto", indices=None):
             dev_tensor(w["q"]), dev_tensor(w["kv"]), dev_tensor(w["block_table"]), dev_tensor(idx),
             page_block=w["page_block"], seqlens_k=dev_tensor(w.get("seqlens_k")),
             s_kv_per_req=w["s_kv_per_req"], s_q_per_req=w["s_q_per_req"], topk_length=dev_tensor(tl),
-            attn_sink=dev_tensor(w["attn_sink"]), sm_scale=w["sm_scale"], d_v=w["d_v"])
+            attn_sink=dev_tensor(w["attn_sink"]), sm_scale=w["sm_scale"], d_v=w["d_v"], n_split=n_split)
     else:
         out = smla.sparse_mla_fwd(dev_tensor(w["q"]), dev_tensor(w["kv"]), dev_tensor(idx),
                                   dev_tensor(tl), dev_tensor(w["attn_sink"]), sm_scale=w["sm_scale"],
-                                  d_v=w["d_v"])
+                                  d_v=w["d_v"], n_split=n_split)
     torch.cuda.synchronize()
     return out
 

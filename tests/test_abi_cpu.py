@@ -23,7 +23,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:smla_status|const char\*|int)\s+(sparse_mla_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:smla_status|const char\*|int|size_t)\s+(sparse_mla_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_expected_entry_points():
@@ -36,8 +36,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.sparse_mla_abi_version() == 1
-    for code in range(7):
+    assert lib.sparse_mla_abi_version() == 2
+    for code in range(8):
         s = smla.sparse_mla_status_string(code)
         assert s and s != "unknown status"
     assert smla.sparse_mla_status_string(99) == "unknown status"
@@ -93,3 +93,25 @@ def test_python_wrapper_rejects_cpu_tensors():
     q = torch.zeros((2, 64, 512), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         smla.sparse_mla_fwd(q, q, torch.zeros((2, 1, 4), dtype=torch.int32))
+
+
+def test_splitkv_workspace_size_and_argument_checks(lib):
+    size = lib.sparse_mla_splitkv_workspace_size
+    assert size(4, 64, 1) == 0                      # one range needs no workspace
+    units = 4 * 2 * 3
+    o_bytes = units * 64 * 512 * 4
+    assert size(4, 128, 3) == ((o_bytes + 255) // 256) * 256 + units * 3 * 64 * 4
+    assert size(4, 64, 0) == 0 and size(4, 64, 65) == 0 and size(4, 48, 2) == 0
+    f = lib.sparse_mla_fwd_splitkv
+
+    def call(n_split=2, ws=FAKE, nbytes=1 << 30, **kw):
+        a = dict(q=FAKE, kv=FAKE, idx=FAKE, out=FAKE, s_q=4, h_q=64, topk=256)
+        a.update(kw)
+        return f(a["q"], a["kv"], a["idx"], None, None, ctypes.c_float(0.04), 512, a["out"], FAKE, FAKE,
+                 a["s_q"], 1000, a["h_q"], 512, a["topk"], n_split, ws, nbytes, None)
+
+    assert call(n_split=0) == 2 and call(n_split=65) == 2
+    assert call(ws=None) == 7                       # missing workspace
+    assert call(nbytes=1000) == 7                   # too small
+    assert call(ws=FAKE + 16) == 3                  # not 256-byte aligned
+    assert call(s_q=0, q=None, kv=None, idx=None, out=None) == 0

@@ -262,3 +262,35 @@ def test_paged_per_request_lengths(with_len):
     # request's length or its block table, and a request with an empty cache
     w = _paged_case(31, with_len=with_len)
     assert_parity(to_np(run_gpu(w)), run_oracle(w), f"paged seqlens len={with_len}")
+
+
+# ---------------------------------------------------------------- split-KV
+@pytest.mark.parametrize("case", CASES, ids=[f"s{c[0]}" for c in CASES])
+@pytest.mark.parametrize("n_split", [2, 5, 64])
+def test_splitkv_matches_oracle(case, n_split):
+    # rows cut into n_split ranges (many of them empty when n_split * 64 > L_t), merged with
+    # log-sum-exp weights; empty rows, sinks, duplicates and poisoned suffixes as in the base case
+    seed, s_q, s_kv, h_q, d_qk, topk = case
+    w = W.random_case(seed, s_q, s_kv, h_q, d_qk, topk, with_len=(n_split != 5), with_sink=True,
+                      poison_suffix=(n_split != 5), dup=(n_split == 5))
+    assert_parity(to_np(run_gpu(w, n_split=n_split)), run_oracle(w), f"{case} n_split={n_split}")
+
+
+@pytest.mark.parametrize("with_len", [True, False])
+def test_splitkv_paged(with_len):
+    w = _paged_case(32, with_len=with_len)
+    assert_parity(to_np(run_gpu(w, n_split=3)), run_oracle(w), f"paged split len={with_len}")
+
+
+def test_splitkv_small_batch_decode_shape():
+    # two requests of two queries each over 2048-slot lists: 8 (row, head group) items, cut
+    # into enough ranges to cover the SMs
+    import sparse_mla_attention_fwd_gb300 as smla
+    w = _paged_case(33, n_req=2, s_q_per_req=2, page=64, max_blocks=64, h_q=128, d_qk=576, topk=2048,
+                    with_len=False)
+    rng = np.random.default_rng(5)
+    idx = np.stack([rng.choice(64 * 64, size=2048, replace=False) for _ in range(4)]).astype(np.int32)
+    w = dict(w, indices=idx.reshape(4, 1, 2048), seqlens_k=None)
+    n = smla.auto_splits(4, 128, 2048)
+    assert n > 1
+    assert_parity(to_np(run_gpu(w, n_split=n)), run_oracle(w), f"small-batch decode n_split={n}")

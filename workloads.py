@@ -205,6 +205,25 @@ def decode(n_req=256, s_kv=4096, h_q=128, d_qk=576, topk=2048, n_valid=1024, pag
     return w
 
 
+def decode_fixed(n_req=2, s_q_per_req=2, s_kv=32768, h_q=128, d_qk=576, topk=2048, page_block=64,
+                 config_no=6):
+    """Small-batch paged decode (the FlashMLA PR #216 "Reproduction" fixed-width sweep shape:
+    S_q=2 queries per request, H=128, s_kv=32768, 64-token pages, top-k 2048): every slot holds
+    a distinct valid position of its request, no topk_length."""
+    rng = rng_for(config_no)
+    max_blocks = (s_kv + page_block - 1) // page_block
+    n_pages = n_req * max_blocks
+    s_q = n_req * s_q_per_req
+    q = normal_bf16(rng, (s_q, h_q, d_qk))
+    pool = normal_bf16(rng, (n_pages * page_block, 1, d_qk))
+    block_table = rng.permutation(n_pages).astype(np.int32).reshape(n_req, max_blocks)
+    idx = distinct_rows(rng, s_q, topk, s_kv)
+    w = _base("decode_fixed", q, pool, idx.reshape(s_q, 1, topk), None, None, s_kv=s_kv)
+    w.update(paged=True, block_table=block_table, page_block=page_block, s_kv_per_req=s_kv,
+             s_q_per_req=s_q_per_req, seqlens_k=None)
+    return w
+
+
 def random_case(seed, s_q, s_kv, h_q, d_qk, topk, with_len=False, with_sink=False,
                 poison_suffix=False, dup=False):
     """Small mixed-pattern case for parity tests: per row one of front-packed / scattered
