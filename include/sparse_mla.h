@@ -133,6 +133,29 @@ smla_status sparse_mla_fwd_paged_splitkv(const void* q, const void* kv_pool, int
                                          smla_stream_t stream);
 
 /*
+ * Allocation-free form of sparse_mla_fwd_paged_splitkv: the split-KV partial results go to a
+ * scratch array that lives in the library itself (a 32 MiB __device__ array per device)
+ * instead of a caller workspace, so the call needs no buffer besides its inputs and outputs.
+ *   - Problems whose partial results do not fit, i.e. sparse_mla_splitkv_workspace_size(s_q,
+ *     h_q, n_split) > 32 MiB (33554432 bytes), are rejected with SMLA_ERR_WORKSPACE before
+ *     anything runs.
+ *   - Nothing in the scratch has to start at zero (every work unit writes its whole partial
+ *     result before the merge reads it), so the call clears nothing.
+ *   - Races: all calls on one device share the one scratch array.  Two calls whose kernels
+ *     may overlap (different streams, or different host threads without ordering) corrupt
+ *     each other's partial results; callers must order them (same stream, or an event or
+ *     synchronisation between them).  Calls on different devices are independent.
+ * With n_split == 1 the scratch is not used.  Other arguments, outputs and errors are as in
+ * sparse_mla_fwd_paged_splitkv.
+ */
+smla_status sparse_mla_fwd_paged_splitkv_static(
+    const void* q, const void* kv_pool, int64_t pool_rows, const int32_t* block_table, int max_blocks,
+    int page_block, const int32_t* seqlens_k, int64_t s_kv_per_req, int s_q_per_req,
+    const int32_t* indices, const int32_t* topk_length, const float* attn_sink, float sm_scale, int d_v,
+    void* out, float* lse, float* max_logits, int64_t s_q, int h_q, int d_qk, int topk, int n_split,
+    smla_stream_t stream);
+
+/*
  * Reads (and, when reset != 0, clears) the device-side status word that kernels set when one
  * of their bounded waits gave up: SMLA_OK or SMLA_ERR_DEVICE_TIMEOUT.  Synchronises with the
  * device (a blocking copy of one int); SMLA_ERR_LAUNCH if that copy fails.

@@ -21,7 +21,8 @@ import torch
 from ._native import EXPORTED, SmlaError, load_library, status_string
 from .native_build import LIB_PATH, build as build_library
 
-__all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "auto_splits", "sparse_mla_device_status",
+__all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_fwd_paged_splitkv_static", "auto_splits",
+           "sparse_mla_device_status",
            "sparse_mla_status_string", "SmlaError", "load_library", "build_library", "LIB_PATH"]
 
 
@@ -184,6 +185,42 @@ def sparse_mla_fwd_paged(q, kv_pool, block_table, indices, page_block=64, seqlen
                 int(h_q), int(d_qk), int(topk), int(n_split), _ptr(ws), int(nbytes), _stream_handle(stream, dev))
     if rc != 0:
         raise SmlaError(rc, "sparse_mla_fwd_paged")
+    return out, lse, max_logits
+
+
+def sparse_mla_fwd_paged_splitkv_static(q, kv_pool, block_table, indices, n_split, page_block=64,
+                                        seqlens_k=None, s_kv_per_req=None, s_q_per_req=1, topk_length=None,
+                                        attn_sink=None, sm_scale=None, d_v=512, out=None, lse=None,
+                                        max_logits=None, stream=None):
+    """Split-KV paged forward whose partial results use the library's own 32 MiB scratch array
+    (no workspace is allocated anywhere).  Calls on one device must not overlap; see the C
+    header."""
+    lib = load_library()
+    _check(q, "q", torch.bfloat16)
+    dev = q.device
+    _check(kv_pool, "kv_pool", torch.bfloat16, dev)
+    _check(block_table, "block_table", torch.int32, dev)
+    _check(indices, "indices", torch.int32, dev)
+    _check(seqlens_k, "seqlens_k", torch.int32, dev)
+    _check(topk_length, "topk_length", torch.int32, dev)
+    _check(attn_sink, "attn_sink", torch.float32, dev)
+    s_q, h_q, d_qk = q.shape
+    pool_rows = kv_pool.shape[0]
+    max_blocks = block_table.shape[1]
+    if s_kv_per_req is None:
+        s_kv_per_req = max_blocks * page_block
+    topk = indices.shape[-1] if indices.dim() else 0
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d_qk)
+    out, lse, max_logits = _outputs(q, h_q, d_v, out, lse, max_logits)
+    with torch.cuda.device(dev):
+        rc = lib.sparse_mla_fwd_paged_splitkv_static(
+            _ptr(q), _ptr(kv_pool), int(pool_rows), _ptr(block_table), int(max_blocks), int(page_block),
+            _ptr(seqlens_k), int(s_kv_per_req), int(s_q_per_req), _ptr(indices), _ptr(topk_length),
+            _ptr(attn_sink), float(sm_scale), int(d_v), _ptr(out), _ptr(lse), _ptr(max_logits), int(s_q),
+            int(h_q), int(d_qk), int(topk), int(n_split), _stream_handle(stream, dev))
+    if rc != 0:
+        raise SmlaError(rc, "sparse_mla_fwd_paged_splitkv_static")
     return out, lse, max_logits
 
 

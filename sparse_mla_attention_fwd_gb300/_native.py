@@ -16,7 +16,8 @@ STATUS_NAMES = {0: "SMLA_OK", 1: "SMLA_ERR_NULL_PTR", 2: "SMLA_ERR_BAD_SHAPE",
                 3: "SMLA_ERR_MISALIGNED", 4: "SMLA_ERR_LAUNCH", 5: "SMLA_ERR_DEVICE_TIMEOUT",
                 6: "SMLA_ERR_TENSOR_MAP", 7: "SMLA_ERR_WORKSPACE"}
 EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_splitkv_workspace_size",
-            "sparse_mla_fwd_splitkv", "sparse_mla_fwd_paged_splitkv", "sparse_mla_device_status",
+            "sparse_mla_fwd_splitkv", "sparse_mla_fwd_paged_splitkv", "sparse_mla_fwd_paged_splitkv_static",
+            "sparse_mla_device_status",
             "sparse_mla_status_string", "sparse_mla_abi_version")
 
 _lock = threading.Lock()
@@ -56,6 +57,9 @@ def load_library(path: str | None = None):
         lib.sparse_mla_fwd_paged_splitkv.restype = I32
         lib.sparse_mla_fwd_paged_splitkv.argtypes = [P, P, I64, P, I32, I32, P, I64, I32, P, P, P, F32, I32,
                                                      P, P, P, I64, I32, I32, I32, I32, P, SZ, P]
+        lib.sparse_mla_fwd_paged_splitkv_static.restype = I32
+        lib.sparse_mla_fwd_paged_splitkv_static.argtypes = [P, P, I64, P, I32, I32, P, I64, I32, P, P, P, F32,
+                                                            I32, P, P, P, I64, I32, I32, I32, I32, P]
         lib.sparse_mla_device_status.restype = I32
         lib.sparse_mla_device_status.argtypes = [I32]
         lib.sparse_mla_status_string.restype = ctypes.c_char_p

@@ -80,6 +80,12 @@ enum : uint32_t { kFirstBlock = 1u, kLastBlock = 2u };
 
 __device__ int g_device_status = 0;    // SMLA_ERR_DEVICE_TIMEOUT once any wait gave up
 
+// Scratch of the allocation-free split-KV entry point (sparse_mla_fwd_paged_splitkv_static):
+// 32 MiB, enough for e.g. 8 rows x 2 head groups x 16 ranges.  Every unit writes its whole
+// partial result before the merge reads it, so no part of it has to start at zero.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) uint8_t g_splitkv_scratch[kStaticScratchBytes];
+
 #ifdef SMLA_TRACE
 // Pipeline trace (debug builds only): SM clock stamps of each block's events in CTA 0.
 constexpr int kTraceBlocks = 256;
@@ -1121,6 +1127,36 @@ smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t poo
   return fwd_paged(q, kv_pool, pool_rows, block_table, max_blocks, page_block, seqlens_k, s_kv_per_req,
                    s_q_per_req, indices, topk_length, attn_sink, sm_scale, d_v, out, lse, max_logits,
                    s_q, h_q, d_qk, topk, 1, nullptr, 0, stream);
+}
+
+smla_status sparse_mla_fwd_paged_splitkv_static(
+    const void* q, const void* kv_pool, int64_t pool_rows, const int32_t* block_table, int max_blocks,
+    int page_block, const int32_t* seqlens_k, int64_t s_kv_per_req, int s_q_per_req,
+    const int32_t* indices, const int32_t* topk_length, const float* attn_sink, float sm_scale, int d_v,
+    void* out, float* lse, float* max_logits, int64_t s_q, int h_q, int d_qk, int topk, int n_split,
+    cudaStream_t stream) {
+  // the scratch is fixed: larger problems are rejected before anything runs
+  if (s_q >= 0 && h_q > 0 && h_q % kGroupHeads == 0 && n_split > 1 && n_split <= kMaxSplit &&
+      splitkv_bytes(s_q, h_q, n_split, nullptr) > kStaticScratchBytes)
+    return SMLA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (n_split > 1 && s_q > 0) {
+    // the scratch's address on the current device, looked up once per device with that device
+    // current (each device has its own copy of the array)
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SMLA_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_splitkv_scratch) != cudaSuccess) {
+      addr[dev] = nullptr;
+      return SMLA_ERR_LAUNCH;
+    }
+    scratch = addr[dev];
+  }
+  return fwd_paged(q, kv_pool, pool_rows, block_table, max_blocks, page_block, seqlens_k, s_kv_per_req,
+                   s_q_per_req, indices, topk_length, attn_sink, sm_scale, d_v, out, lse, max_logits,
+                   s_q, h_q, d_qk, topk, n_split, scratch, kStaticScratchBytes, stream);
 }
 
 size_t sparse_mla_splitkv_workspace_size(int64_t s_q, int h_q, int n_split) {
