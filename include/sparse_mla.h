@@ -162,6 +162,15 @@ smla_status sparse_mla_fwd_paged_splitkv_static(
  */
 smla_status sparse_mla_device_status(int reset);
 
+/*
+ * Diagnostic of the failure-detection path: launches a one-thread kernel that runs the same
+ * bounded mbarrier wait the forward kernels use, on a barrier nothing ever completes.  After
+ * limit_ns (1 .. 2e9 ns) of device time the wait gives up, the kernel sets the status word to
+ * SMLA_ERR_DEVICE_TIMEOUT and returns; the context stays usable.  Read the result with
+ * sparse_mla_device_status after synchronising.  SMLA_ERR_BAD_SHAPE for a limit out of range.
+ */
+smla_status sparse_mla_selftest_wait_timeout(uint64_t limit_ns, smla_stream_t stream);
+
 /* Static, human-readable description of a status code.  Never NULL. */
 const char* sparse_mla_status_string(smla_status status);
 

@@ -878,6 +878,20 @@ __global__ void __launch_bounds__(kMergeThreads)
   }
 }
 
+// ------------------------------------------------------------------------ wait self-test
+// Runs the bounded mbarrier wait every role of the forward uses on a barrier that nothing will
+// ever complete: the wait gives up after limit_ns, the kernel records SMLA_ERR_DEVICE_TIMEOUT
+// in the status word and returns.  No copies, MMAs or tensor memory are involved.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  wait_or_flag(smem_u32(&bar), 0, &abort_flag, limit_ns);
+}
+
 // ------------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1157,6 +1171,12 @@ smla_status sparse_mla_fwd_paged_splitkv_static(
   return fwd_paged(q, kv_pool, pool_rows, block_table, max_blocks, page_block, seqlens_k, s_kv_per_req,
                    s_q_per_req, indices, topk_length, attn_sink, sm_scale, d_v, out, lse, max_logits,
                    s_q, h_q, d_qk, topk, n_split, scratch, kStaticScratchBytes, stream);
+}
+
+smla_status sparse_mla_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns == 0 || limit_ns > kDefaultWaitLimitNs) return SMLA_ERR_BAD_SHAPE;
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
 }
 
 size_t sparse_mla_splitkv_workspace_size(int64_t s_q, int h_q, int n_split) {

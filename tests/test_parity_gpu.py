@@ -182,6 +182,22 @@ def test_decode_fixed_equals_dynamic():
     torch.testing.assert_close(a[1], b[1], atol=1e-6, rtol=8.01 / 65536)
 
 
+def test_bounded_wait_times_out_and_reports_it():
+    # failure detection without a fault: a wait on a barrier nothing completes gives up after
+    # 20 ms, the status word says so, and the context still runs the forward correctly
+    import sparse_mla_attention_fwd_gb300 as smla
+    from sparse_mla_attention_fwd_gb300 import _native
+    lib = _native.load_library()
+    assert smla.sparse_mla_device_status(reset=True) == 0
+    assert lib.sparse_mla_selftest_wait_timeout(20_000_000, None) == 0
+    torch.cuda.synchronize()
+    assert smla.sparse_mla_device_status(reset=True) == 5      # SMLA_ERR_DEVICE_TIMEOUT
+    assert smla.sparse_mla_device_status() == 0
+    w = W.tiny(with_len=True, with_sink=True)
+    assert_parity(to_np(run_gpu(w)), run_oracle(w), "tiny after a timeout")
+    assert lib.sparse_mla_selftest_wait_timeout(0, None) == 2
+
+
 def test_no_device_timeouts_recorded():
     import sparse_mla_attention_fwd_gb300 as smla
     assert smla.sparse_mla_device_status() == 0
