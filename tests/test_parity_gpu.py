@@ -310,3 +310,23 @@ def test_splitkv_small_batch_decode_shape():
     n = smla.auto_splits(4, 128, 2048)
     assert n > 1
     assert_parity(to_np(run_gpu(w, n_split=n)), run_oracle(w), f"small-batch decode n_split={n}")
+
+
+# ---------------------------------------------------------------- randomized sweep
+def _sweep_case(k):
+    rng = np.random.default_rng(9000 + k)
+    h_q = int(rng.choice([64, 128, 192, 256]))
+    d_qk = int(rng.choice([512, 576]))
+    s_q = int(rng.integers(1, 12))
+    topk = int(rng.integers(1, 1400))
+    s_kv = int(rng.integers(1, 3000))
+    w = W.random_case(9100 + k, s_q, s_kv, h_q, d_qk, topk, with_len=bool(k % 2), with_sink=bool(k % 3 == 0),
+                      poison_suffix=bool(k % 2), dup=bool(k % 5 == 0))
+    n_split = int(rng.choice([1, 1, 2, 3, 7]))
+    return w, n_split
+
+
+@pytest.mark.parametrize("k", range(24))
+def test_randomized_sweep(k):
+    w, n_split = _sweep_case(k)
+    assert_parity(to_np(run_gpu(w, n_split=n_split)), run_oracle(w), f"sweep {k} n_split={n_split}")
