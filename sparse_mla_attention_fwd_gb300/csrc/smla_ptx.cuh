@@ -170,7 +170,9 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T.
+// D[tmem] (+)= A[tmem] * B[smem]^T.  A (M = 128, kind::f16) sits in TMEM with row m in lane m
+// and elements k = 2c (low half) and 2c+1 (high half) in column c; one K = 16 step reads 8
+// columns.
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -370,6 +372,37 @@ __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]
   asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(taddr));
+}
+
+// Store counterpart of tmem_ld_16x256b (same thread -> lane / column mapping).
+__device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, uint32_t r0, uint32_t r1,
+                                                uint32_t r2, uint32_t r3) {
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
+// 16 lanes x 128 bits, 8 repetitions along the columns (32 columns): thread t stores r[2i] to
+// lane (t>>2), column 4i + (t&3) and r[2i+1] to lane (t>>2)+8, same column.
+__device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+// Four 8x8 b16 matrices, transposed on load.  Threads 8j..8j+7 give the row addresses (16
+// bytes each) of matrix j; thread t receives in r[j] the elements at rows 2(t&3) (low half)
+// and 2(t&3)+1 (high half) of column t>>2 of matrix j.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(saddr)
+               : "memory");
 }
 
 }  // namespace smla

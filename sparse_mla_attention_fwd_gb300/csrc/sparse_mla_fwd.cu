@@ -29,13 +29,19 @@
 //   warp 10             scheduler : per row, one pass over its index list that packs the
 //                                   counted slots into 64-slot blocks (resolved TMA row
 //                                   coordinates + validity mask + first/last flags) in a shared
-//                                   8-deep ring.  It runs ahead, so index loads never sit on the
-//                                   critical path.
+//                                   16-deep ring.  It runs ahead, so index loads never sit on
+//                                   the critical path.
+// With d_qk = 512 a fourth warpgroup (warps 12-15, 512 threads) copies value columns 0..255 of
+// each gathered block into TMEM as V^T and also issues gathers; setmaxnreg gives the softmax
+// warpgroup 200 registers and the others 104.
 // Tensor-core work per 64-key block:
 //   S[64 heads x 64 keys]  = Q_g . K_blk^T        (M=64, N=64, K=d_qk; both K-major SW128)
 //   O^T[512 x 64 heads]   += V_blk^T . P^T        (4 x M=128, N=64, K=64; V^T read MN-major
-//                                                  straight out of the gathered K block)
-// TMEM: O^T in columns [0,256), S double buffer in [256,384).
+//                                                  straight out of the gathered block, or for
+//                                                  value columns 0..255 with d_qk = 512, out
+//                                                  of TMEM)
+// TMEM: O^T in columns [0,256), S double buffer in [256,384), with d_qk = 512 a V^T double
+// buffer (value columns 0..255) in [384,512).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -62,16 +68,25 @@ constexpr int kDv = 512;               // value width (first d_v columns of each
 // issuer leaves between chains (it is blocked inside each chain's issue until the chain has
 // nearly drained, then has to find the next ready chain).
 constexpr int kThreads = 384;
+// d_qk = 512 adds a fourth warpgroup (warps 12-15, TMEM lane quadrants 0-3) that copies V^T
+// into TMEM; registers are then rebalanced towards the softmax warpgroup.
+template <int D_QK>
+constexpr int threads_for() { return D_QK == 512 ? 512 : kThreads; }
+constexpr int kVtWarp0 = 12;
+constexpr int kSoftmaxRegs = 200;      // setmaxnreg split of the 512-thread kernel: 128 x 200
+constexpr int kOtherRegs = 104;        // + 384 x 104 = 65536 = 512 threads x 128 at launch
 constexpr int kGatherWarps = 5;        // warps 0, 1, 3, 8, 9
 constexpr int kSoftmaxWarp0 = 4;       // warps 4-7 (TMEM lane quadrants 0-3)
 constexpr int kQkWarp = 2;             // QK issuer; also allocates TMEM and loads Q tiles
 constexpr int kPvWarp = 11;            // PV issuer
 constexpr int kSchedWarp = 10;
-constexpr int kRing = 8;               // scheduler ring depth (blocks)
+constexpr int kRing = 16;              // scheduler ring depth (blocks)
 constexpr int kRingConsumers = kGatherWarps + 4 + 2;   // arrivals that free a ring slot
+constexpr int kRingConsumersVT = kRingConsumers + 4;   // ... with the V^T warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O^T: 4 chunks x 64 columns
 constexpr uint32_t kTmemS = 256;       // S buffers: 256 + 64*b
+constexpr uint32_t kTmemVT = 384;      // d_qk = 512: V^T of value chunks 0-1, 2 buffers x 2 x 32
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the running max grows by > 2^8
@@ -91,7 +106,7 @@ static __device__ __align__(256) uint8_t g_splitkv_scratch[kStaticScratchBytes];
 constexpr int kTraceBlocks = 256;
 enum TraceEvent {
   kTrRing, kTrGatherIssue, kTrQkIssue, kTrSReady, kTrPReady, kTrPvIssue, kTrEpilogue,
-  kTrSLoaded, kTrSent, kTrRecv, kTrMath, kTrBar, kTrEvents
+  kTrSLoaded, kTrSent, kTrVtStart, kTrVtWait0, kTrVtEnd, kTrEvents
 };
 __device__ long long g_trace[kTraceBlocks][kTrEvents];
 __device__ __forceinline__ void trace(int64_t b, int ev) {
@@ -197,7 +212,7 @@ __device__ __forceinline__ int kv_row_of(const FwdParams& p, int64_t t, int v) {
 // SPLIT: work units are (item, slot range); the epilogue writes the unit's partial result to
 // the split-KV workspace instead of O / lse / max_logits (a second kernel merges the ranges).
 template <int D_QK, bool DYNAMIC, bool PAGED, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for<D_QK>(), 1)
     sparse_mla_fwd_kernel(const __grid_constant__ CUtensorMap q_map,
                           const __grid_constant__ CUtensorMap kv_map, const FwdParams p) {
   constexpr int kChunks = D_QK / 64;                 // 128-byte column chunks of a row
@@ -212,6 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // columns, so group g of a stage is refilled as soon as PV M-chunk g of the block before has
   // completed, and S = QK^T of the new block starts on group 0 while later groups are in flight.
   constexpr int kGroups = 4;
+  // With d_qk = 512 (no rope chunk) PV reads value chunks 0-1 (columns 0..255) as V^T out of
+  // TMEM, double-buffered in the 128 columns that O^T and S leave free; chunks 2-3 it reads
+  // from the stage as usual.  The V^T warps copy column groups 0-1 of a stage into TMEM
+  // (ldmatrix.trans -> tcgen05.st) as soon as they land, so those groups are released once
+  // S = QK^T and the copy have read them, well before PV; the gather of groups 0-1 of block
+  // b+2 then overlaps PV of block b, and QK(b+2) streams through them while groups 2-3 are in
+  // flight.  (With a rope chunk the stage also holds P^T, so it stays until PV ends.)
+  constexpr bool kVT = (kChunks == 8);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -225,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_kv_full[2][kGroups], bar_kv_empty[2][kGroups];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2], bar_o_free;
   __shared__ __align__(8) uint64_t bar_final_qk, bar_final_pv;
+  __shared__ __align__(8) uint64_t bar_vt_full[2][2], bar_vt_free[2][2];   // [buffer][chunk]
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ float s_alpha[kGroupHeads];
@@ -250,14 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_flag = 0;
     for (int r = 0; r < kRing; ++r) {
       mbar_init(smem_u32(&bar_ring_full[r]), 1);
-      mbar_init(smem_u32(&bar_ring_empty[r]), kRingConsumers);
+      mbar_init(smem_u32(&bar_ring_empty[r]), kVT ? kRingConsumersVT : kRingConsumers);
     }
     mbar_init(smem_u32(&bar_q_full), 1);
     mbar_init(smem_u32(&bar_q_empty), 1);
     for (int s = 0; s < 2; ++s) {
       for (int g = 0; g < kGroups; ++g) {
         mbar_init(smem_u32(&bar_kv_full[s][g]), 1);
-        mbar_init(smem_u32(&bar_kv_empty[s][g]), 1);
+        // released by PV (one commit), or for groups 0-1 with V^T in TMEM by S = QK^T (one
+        // commit) and the four V^T warps
+        mbar_init(smem_u32(&bar_kv_empty[s][g]), (kVT && g < 2) ? 5 : 1);
       }
       mbar_init(smem_u32(&bar_s_full[s]), 1);
       mbar_init(smem_u32(&bar_p_full[s]), 128);
@@ -266,6 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bar_o_free), 128);
     mbar_init(smem_u32(&bar_final_qk), 1);
     mbar_init(smem_u32(&bar_final_pv), 1);
+    for (int v = 0; v < 4; ++v) {
+      mbar_init(smem_u32(&bar_vt_full[v >> 1][v & 1]), 4);
+      mbar_init(smem_u32(&bar_vt_free[v >> 1][v & 1]), 1);
+    }
     fence_mbar_init();
   }
   if (warp == kQkWarp) {
@@ -277,194 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == kSchedWarp) {
-    // ======================================================== scheduler
-    // Per row, a parallel scan first finds the last counted slot (j < L_t, 0 <= idx < s_kv) and
-    // the number of counted slots.  A row whose counted slots form a dense prefix (the usual
-    // case: front-packed lists, -1 or INT_MAX padding) is cut into blocks straight from its
-    // slot list, so trailing padding costs nothing (FlashMLA PR #196, "Fix").  Any other row is
-    // packed: its counted slots go, in slot order, into dense blocks, so invalid entries inside
-    // the row cost nothing either.  The result does not depend on the packing (it is invariant
-    // under permuting slots and inserting invalid ones; the oracle's pins check both).  A row
-    // costs max(ceil(n_counted / 64), 1) blocks, and every role walks the same block stream.
-    const uint32_t lanes_below = (1u << lane) - 1u;
-    auto acquire = [&](int64_t blk) {
-      if (blk >= kRing)
-        wait_or_flag(smem_u32(&bar_ring_empty[blk % kRing]), ((blk / kRing) - 1) & 1, abort, lim);
-    };
-    auto publish = [&](int64_t blk, uint32_t m0, uint32_t m1, uint32_t flags, int64_t item) {
-      const int r = static_cast<int>(blk % kRing);
-      if (lane == 0) {
-        ring[r].mask[0] = m0;
-        ring[r].mask[1] = m1;
-        ring[r].item = static_cast<int32_t>(item);
-        ring[r].flags = flags;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        SMLA_TRACE_EVENT(blk, kTrRing);
-        mbar_arrive(smem_u32(&bar_ring_full[r]));
-      }
-    };
-    int64_t b = 0;
-    for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-      const int64_t unit = blockIdx.x + i * gridDim.x;
-      const int64_t item = unit;   // what the ring carries: the unit (the item itself unless SPLIT)
-      const int64_t t = item_of_unit(unit) / p.n_groups;
-      const int32_t* idx_row = p.indices + t * static_cast<int64_t>(p.topk);
-      const int64_t kv_len = row_kv_len<PAGED>(p, t);
-      int Lr = DYNAMIC ? min(max(__ldg(p.topk_length + t), 0), p.topk) : p.topk;
-      if constexpr (SPLIT) {
-        // this unit's share of the row: range `split` of n_split 64-aligned ranges of [0, L_t)
-        const int split = static_cast<int>(unit % p.n_split);
-        const int span = ((Lr + p.n_split - 1) / p.n_split + kBlockN - 1) / kBlockN * kBlockN;
-        const int j0 = min(split * span, Lr);
-        idx_row += j0;
-        Lr = min(Lr - j0, span);
-      }
-      int last = -1, cnt = 0;
-      if constexpr (PAGED) {
-        // Decode-shaped work has few blocks per CTA, so the scan's load latency is exposed:
-        // pull the next row's list into L2 and keep eight 32-slot chunks of loads in flight.
-        // (On the prefill paths, which are throughput-bound, this form measured slower.)
-        if (i + 1 < n_my_items) {
-          const int64_t tn = item_of_unit(unit + gridDim.x) / p.n_groups;
-          const char* nrow = reinterpret_cast<const char*>(p.indices + tn * static_cast<int64_t>(p.topk));
-          for (int off = lane * 128; off < p.topk * 4; off += 32 * 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + off));
-        }
-        for (int j0 = 0; j0 < Lr; j0 += 8 * 32) {
-          int vals[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = j0 + 32 * u + lane;
-            vals[u] = j < Lr ? __ldg(idx_row + j) : -1;
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = j0 + 32 * u + lane;
-            if (j < Lr && slot_ok<PAGED>(p, vals[u], kv_len)) {
-              last = j;
-              ++cnt;
-            }
-          }
-        }
-      } else {
-        for (int j = lane; j < Lr; j += 32)
-          if (slot_ok<PAGED>(p, __ldg(idx_row + j), kv_len)) {
-            last = j;
-            ++cnt;
-          }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      }
-      const int L = last + 1;
-      if (cnt == L) {
-        // dense prefix: block k holds slots 64k .. 64k+63 of the list
-        const int nblk = max((L + kBlockN - 1) / kBlockN, 1);
-        for (int k = 0; k < nblk && !*abort; ++k, ++b) {
-          const int r = static_cast<int>(b % kRing);
-          acquire(b);
-          uint32_t m[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int slot = k * kBlockN + 32 * h + lane;
-            int coord = -1;
-            if (slot < L) {
-              const int v = __ldg(idx_row + slot);
-              if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
-            }
-            ring[r].rows[32 * h + lane] = coord;
-            m[h] = __ballot_sync(0xffffffffu, coord >= 0);
-          }
-          publish(b, m[0], m[1], (k == 0 ? kFirstBlock : 0u) | (k == nblk - 1 ? kLastBlock : 0u), item);
-        }
-        continue;
-      }
-      // packing pass over [0, L): the indices were just read and come from L1
-      const int64_t b0 = b;
-      int count = 0;               // counted slots packed so far
-      int64_t acquired = b0 - 1;   // last block whose ring slot is held
-      int64_t published = b0;      // next block to publish
-      for (int j0 = 0; j0 < L && !*abort; j0 += 32) {
-        const int slot = j0 + lane;
-        int coord = -1;
-        if (slot < L) {
-          const int v = __ldg(idx_row + slot);
-          if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
-        }
-        const uint32_t bal = __ballot_sync(0xffffffffu, coord >= 0);
-        if (bal == 0u) continue;
-        const int n = __popc(bal);
-        const int64_t newest = b0 + (count + n - 1) / kBlockN;   // block of the newest slot
-        while (acquired < newest) acquire(++acquired);
-        if (coord >= 0) {
-          const int pos = count + __popc(bal & lanes_below);
-          ring[(b0 + pos / kBlockN) % kRing].rows[pos % kBlockN] = coord;
-        }
-        count += n;
-        __syncwarp();
-        // every block before the newest one is full and has a successor
-        for (; published < newest; ++published)
-          publish(published, 0xffffffffu, 0xffffffffu, published == b0 ? kFirstBlock : 0u, item);
-      }
-      // the block that holds the row's last counted slot (or one empty block) closes the item
-      if (count == 0) acquire(++acquired);
-      const int64_t lastb = b0 + (count > 0 ? (count - 1) / kBlockN : 0);
-      const int fill = count - static_cast<int>(lastb - b0) * kBlockN;   // 0..64 slots used
-      const int rl = static_cast<int>(lastb % kRing);
-      for (int e = fill + lane; e < kBlockN; e += 32) ring[rl].rows[e] = -1;
-      const uint32_t m0 = fill >= 32 ? 0xffffffffu : ((1u << fill) - 1u);
-      const uint32_t m1 = fill >= 64 ? 0xffffffffu : (fill > 32 ? ((1u << (fill - 32)) - 1u) : 0u);
-      __syncwarp();
-      publish(lastb, m0, m1, (lastb == b0 ? kFirstBlock : 0u) | kLastBlock, item);
-      b = lastb + 1;
-    }
-  } else if (warp < 2 || warp == 3 || warp == 8 || warp == 9) {
-    // ======================================================== gather
-    // TMA issue throughput grows with the number of issuing warps, so the 16 x (chunks of a
-    // group) gather4 items of each column group are dealt round-robin over the 5 gather warps.
-    const int gw = warp < 2 ? warp : (warp == 3 ? 2 : warp - 5);   // 0..4
-    const int it = gw + kGatherWarps * lane;        // item within a group: (4-row group, chunk)
-    const int grp = it & 15;
-    const bool leader = (gw == 0 && lane == 0);
-    int64_t b = 0;
-    for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-      for (bool more = true; more && !*abort; ++b) {
-        const int r = static_cast<int>(b % kRing);
-        const int s = static_cast<int>(b & 1);
-        wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
-        more = (ring[r].flags & kLastBlock) == 0;
-        const int4 rr = *reinterpret_cast<const int4*>(&ring[r].rows[4 * grp]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_ring_empty[r]));
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          const int c0 = 2 * g;
-          const int nch = (g == kGroups - 1) ? kChunks - c0 : 2;
-          if (b >= 2) wait_or_flag(smem_u32(&bar_kv_empty[s][g]), ((b >> 1) - 1) & 1, abort, lim);
-          if (leader) {
-            if (g == 0) SMLA_TRACE_EVENT(b, kTrGatherIssue);
-            mbar_arrive_expect_tx(smem_u32(&bar_kv_full[s][g]), nch * 8192u);
-          }
-          if (it < 16 * nch) {
-            const int chunk = c0 + (it >> 4);
-            tma_gather4(smem_u32(sKV + s * kTileBytes + chunk * 8192 + grp * 512), &kv_map, 64 * chunk,
-                        rr.x, rr.y, rr.z, rr.w, smem_u32(&bar_kv_full[s][g]));
-          }
-        }
-      }
-    }
-    // drain: the last fills of both stages have landed before this CTA may exit
-    if (leader) {
-      for (int64_t bb = (b >= 2 ? b - 2 : 0); bb < b; ++bb)
-        for (int g = 0; g < kGroups; ++g)
-          wait_drain(smem_u32(&bar_kv_full[bb & 1][g]), (bb >> 1) & 1, lim);
-    }
-  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+  // Roles.  The softmax warpgroup comes first so that, in the 512-thread kernel, its code is
+  // dominated by the register increase and every other role by the decrease.
+  if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+    if constexpr (kVT) reg_alloc<kSoftmaxRegs>();
     // ======================================================== softmax / correction / epilogue
     const int q = warp - kSoftmaxWarp0;          // TMEM lane quadrant 0..3
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -548,16 +394,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P as bf16 into the P^T operand tile ([64 heads][64 keys], 128-byte swizzle).  Its
         // previous user (block b-2) finished its PV before the stage was refilled for block b,
-        // which S(b) being ready already implies.  Masked slots hold -inf and give
-        // exp2(-inf) = 0; a row whose offset is still -inf has no valid slot yet, and any finite
-        // offset then yields 0 as well.
+        // which S(b) being ready already implies -- except with V^T in TMEM, where PV's last
+        // M-chunks read TMEM and not the stage, so PV(b-2) is waited for here.  Masked slots hold
+        // -inf and give exp2(-inf) = 0; a row whose offset is still -inf has no valid slot yet,
+        // and any finite offset then yields 0 as well.
+        if (kVT && b >= 2) wait_or_flag(smem_u32(&bar_o_done[sb]), ((b - 2) >> 1) & 1, abort, lim);
         const float neg_m0 = m_used[0] == -INFINITY ? 0.f : -m_used[0];
         const float neg_m1 = m_used[1] == -INFINITY ? 0.f : -m_used[1];
         uint8_t* ptile = p_addr(static_cast<int>(b));
-        uint8_t* prowA = ptile + hA * 128 + 2 * cpair;
-        uint8_t* prowB = ptile + hB * 128 + 2 * cpair;
         const int swA = hA & 7, swB = hB & 7;
         float ls[2] = {0.f, 0.f};
+        uint8_t* prowA = ptile + hA * 128 + 2 * cpair;
+        uint8_t* prowB = ptile + hB * 128 + 2 * cpair;
 #pragma unroll
         for (int i8 = 0; i8 < 8; ++i8) {
           const float p0 = fast_exp2(fmaf(sv[4 * i8], c, neg_m0));
@@ -681,111 +529,384 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kQkWarp) {
-    // ======================================================== QK issuer (and Q tile loads)
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_bf16(64, kBlockN, false, false);
-      const uint64_t qd0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint32_t kv_base = smem_u32(sKV);
-      auto load_q = [&](int64_t i) {
-        const int64_t item = item_of_unit(blockIdx.x + i * gridDim.x);
-        const int64_t t = item / p.n_groups;
-        const int g = static_cast<int>(item % p.n_groups);
-        mbar_arrive_expect_tx(smem_u32(&bar_q_full), kTileBytes);
-        const int qrow = static_cast<int>(t * p.h_q + g * kGroupHeads);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, qrow, smem_u32(&bar_q_full));
+  } else {
+    if constexpr (kVT) reg_dealloc<kOtherRegs>();
+    if (warp == kSchedWarp) {
+      // ======================================================== scheduler
+      // Per row, a parallel scan first finds the last counted slot (j < L_t, 0 <= idx < s_kv) and
+      // the number of counted slots.  A row whose counted slots form a dense prefix (the usual
+      // case: front-packed lists, -1 or INT_MAX padding) is cut into blocks straight from its
+      // slot list, so trailing padding costs nothing (FlashMLA PR #196, "Fix").  Any other row is
+      // packed: its counted slots go, in slot order, into dense blocks, so invalid entries inside
+      // the row cost nothing either.  The result does not depend on the packing (it is invariant
+      // under permuting slots and inserting invalid ones; the oracle's pins check both).  A row
+      // costs max(ceil(n_counted / 64), 1) blocks, and every role walks the same block stream.
+      const uint32_t lanes_below = (1u << lane) - 1u;
+      auto acquire = [&](int64_t blk) {
+        if (blk >= kRing)
+          wait_or_flag(smem_u32(&bar_ring_empty[blk % kRing]), ((blk / kRing) - 1) & 1, abort, lim);
       };
-      int64_t q_loaded = 0;                      // Q tiles requested so far
-      if (n_my_items > 0) {
-        load_q(0);
-        q_loaded = 1;
-      }
+      auto publish = [&](int64_t blk, uint32_t m0, uint32_t m1, uint32_t flags, int64_t item) {
+        const int r = static_cast<int>(blk % kRing);
+        if (lane == 0) {
+          ring[r].mask[0] = m0;
+          ring[r].mask[1] = m1;
+          ring[r].item = static_cast<int32_t>(item);
+          ring[r].flags = flags;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          SMLA_TRACE_EVENT(blk, kTrRing);
+          mbar_arrive(smem_u32(&bar_ring_full[r]));
+        }
+      };
       int64_t b = 0;
       for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-        wait_or_flag(smem_u32(&bar_q_full), i & 1, abort, lim);
+        const int64_t unit = blockIdx.x + i * gridDim.x;
+        const int64_t item = unit;   // what the ring carries: the unit (the item itself unless SPLIT)
+        const int64_t t = item_of_unit(unit) / p.n_groups;
+        const int32_t* idx_row = p.indices + t * static_cast<int64_t>(p.topk);
+        const int64_t kv_len = row_kv_len<PAGED>(p, t);
+        int Lr = DYNAMIC ? min(max(__ldg(p.topk_length + t), 0), p.topk) : p.topk;
+        if constexpr (SPLIT) {
+          // this unit's share of the row: range `split` of n_split 64-aligned ranges of [0, L_t)
+          const int split = static_cast<int>(unit % p.n_split);
+          const int span = ((Lr + p.n_split - 1) / p.n_split + kBlockN - 1) / kBlockN * kBlockN;
+          const int j0 = min(split * span, Lr);
+          idx_row += j0;
+          Lr = min(Lr - j0, span);
+        }
+        int last = -1, cnt = 0;
+        if constexpr (PAGED) {
+          // Decode-shaped work has few blocks per CTA, so the scan's load latency is exposed:
+          // pull the next row's list into L2 and keep eight 32-slot chunks of loads in flight.
+          // (On the prefill paths, which are throughput-bound, this form measured slower.)
+          if (i + 1 < n_my_items) {
+            const int64_t tn = item_of_unit(unit + gridDim.x) / p.n_groups;
+            const char* nrow = reinterpret_cast<const char*>(p.indices + tn * static_cast<int64_t>(p.topk));
+            for (int off = lane * 128; off < p.topk * 4; off += 32 * 128)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + off));
+          }
+          for (int j0 = 0; j0 < Lr; j0 += 8 * 32) {
+            int vals[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = j0 + 32 * u + lane;
+              vals[u] = j < Lr ? __ldg(idx_row + j) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = j0 + 32 * u + lane;
+              if (j < Lr && slot_ok<PAGED>(p, vals[u], kv_len)) {
+                last = j;
+                ++cnt;
+              }
+            }
+          }
+        } else {
+          for (int j = lane; j < Lr; j += 32)
+            if (slot_ok<PAGED>(p, __ldg(idx_row + j), kv_len)) {
+              last = j;
+              ++cnt;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+          cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        }
+        const int L = last + 1;
+        if (cnt == L) {
+          // dense prefix: block k holds slots 64k .. 64k+63 of the list
+          const int nblk = max((L + kBlockN - 1) / kBlockN, 1);
+          for (int k = 0; k < nblk && !*abort; ++k, ++b) {
+            const int r = static_cast<int>(b % kRing);
+            acquire(b);
+            uint32_t m[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int slot = k * kBlockN + 32 * h + lane;
+              int coord = -1;
+              if (slot < L) {
+                const int v = __ldg(idx_row + slot);
+                if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+              }
+              ring[r].rows[32 * h + lane] = coord;
+              m[h] = __ballot_sync(0xffffffffu, coord >= 0);
+            }
+            publish(b, m[0], m[1], (k == 0 ? kFirstBlock : 0u) | (k == nblk - 1 ? kLastBlock : 0u), item);
+          }
+          continue;
+        }
+        // packing pass over [0, L): the indices were just read and come from L1
+        const int64_t b0 = b;
+        int count = 0;               // counted slots packed so far
+        int64_t acquired = b0 - 1;   // last block whose ring slot is held
+        int64_t published = b0;      // next block to publish
+        for (int j0 = 0; j0 < L && !*abort; j0 += 32) {
+          const int slot = j0 + lane;
+          int coord = -1;
+          if (slot < L) {
+            const int v = __ldg(idx_row + slot);
+            if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+          }
+          const uint32_t bal = __ballot_sync(0xffffffffu, coord >= 0);
+          if (bal == 0u) continue;
+          const int n = __popc(bal);
+          const int64_t newest = b0 + (count + n - 1) / kBlockN;   // block of the newest slot
+          while (acquired < newest) acquire(++acquired);
+          if (coord >= 0) {
+            const int pos = count + __popc(bal & lanes_below);
+            ring[(b0 + pos / kBlockN) % kRing].rows[pos % kBlockN] = coord;
+          }
+          count += n;
+          __syncwarp();
+          // every block before the newest one is full and has a successor
+          for (; published < newest; ++published)
+            publish(published, 0xffffffffu, 0xffffffffu, published == b0 ? kFirstBlock : 0u, item);
+        }
+        // the block that holds the row's last counted slot (or one empty block) closes the item
+        if (count == 0) acquire(++acquired);
+        const int64_t lastb = b0 + (count > 0 ? (count - 1) / kBlockN : 0);
+        const int fill = count - static_cast<int>(lastb - b0) * kBlockN;   // 0..64 slots used
+        const int rl = static_cast<int>(lastb % kRing);
+        for (int e = fill + lane; e < kBlockN; e += 32) ring[rl].rows[e] = -1;
+        const uint32_t m0 = fill >= 32 ? 0xffffffffu : ((1u << fill) - 1u);
+        const uint32_t m1 = fill >= 64 ? 0xffffffffu : (fill > 32 ? ((1u << (fill - 32)) - 1u) : 0u);
+        __syncwarp();
+        publish(lastb, m0, m1, (lastb == b0 ? kFirstBlock : 0u) | kLastBlock, item);
+        b = lastb + 1;
+      }
+    } else if (warp < 2 || warp == 3 || warp == 8 || warp == 9 || (kVT && warp >= kVtWarp0)) {
+      // ======================================================== gather (+ V^T copies)
+      // TMA issue throughput grows with the number of issuing warps, so the 16 x (chunks of a
+      // group) gather4 items of each column group are dealt round-robin over the gather warps:
+      // warps 0, 1, 3, 8, 9, and with d_qk = 512 also the four V^T warps 12-15.
+      constexpr int kGW = kVT ? kGatherWarps + 4 : kGatherWarps;
+      // gather warp index 0..kGW-1: warps 0, 1, 3, 8, 9 -> 0..4, warps 12-15 -> 5..8
+      const int gw = warp < 2 ? warp
+                   : warp == 3 ? 2
+                   : warp < kVtWarp0 ? warp - 5
+                                     : warp - kVtWarp0 + kGatherWarps;
+      const int it = gw + kGW * lane;                 // item within a group: (4-row group, chunk)
+      const int grp = it & 15;
+      const bool leader = (gw == 0 && lane == 0);
+      // V^T copies (warps 12-15 only).  Warp 12+q fills TMEM lanes 32q..32q+31 of V^T chunks
+      // 0-1 (value columns 128m..128m+127 = column group m of the stage) in buffer j&1.  For
+      // each 16-row half hh and 16-key step x, ldmatrix.trans loads matrix i = keys 16x + 8(i>>1)
+      // + 0..7 by columns 128m + 32q + 16hh + 8(i&1) + 0..7 (eight rows of distinct swizzle
+      // phase: no bank conflicts); thread t then holds keys 16x + 8(i>>1) + 2(t&3) + {0,1} of
+      // column (t>>2) (+8 for odd i), which is exactly what a 16x128b store puts at K positions
+      // 2c, 2c+1 of TMEM column c = 8x + 4(i>>1) + (t&3): natural key order.  The copy of block
+      // j comes in the middle of this warp's gathers for block j+1 and before those for block
+      // j+2, which wait for it (through kv_empty).
+      const bool vt_warp = kVT && warp >= kVtWarp0;
+      auto copy_vt = [&](int64_t j) {
+        const int q = warp - kVtWarp0;
+        const int mat = lane >> 3, rr = lane & 7;
+        const int s = static_cast<int>(j & 1);
+        const uint32_t stage = smem_u32(sKV + s * kTileBytes) + (q >> 1) * 8192 +
+                               static_cast<uint32_t>((8 * (mat >> 1) + rr) * 128);
+        SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, j, kTrVtStart);
+#pragma unroll 1
+        for (int m = 0; m < 2; ++m) {
+          // block j's group m has landed; PV of block j-2 has read V^T buffer j&1, chunk m
+          wait_or_flag(smem_u32(&bar_kv_full[s][m]), (j >> 1) & 1, abort, lim);
+          if (j >= 2) wait_or_flag(smem_u32(&bar_vt_free[s][m]), ((j - 2) >> 1) & 1, abort, lim);
+          SMLA_TRACE_EVENT_IF(m == 0 && q == 0 && lane == 0, j, kTrVtWait0);
+          tc_fence_after();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int u = 4 * (q & 1) + 2 * hh + (mat & 1);
+            const uint32_t a0 = stage + 2 * m * 8192 + ((u ^ rr) << 4);
+            uint32_t rg[16];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              ldsm_x4_trans(a0 + 2048 * x, rg[4 * x], rg[4 * x + 1], rg[4 * x + 2], rg[4 * x + 3]);
+            const uint32_t lanes = static_cast<uint32_t>(32 * q + 16 * hh) << 16;
+            tmem_st_16x128b_x8(tmem + lanes + kTmemVT + 64 * s + 32 * m, rg);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&bar_vt_full[s][m]));
+            mbar_arrive(smem_u32(&bar_kv_empty[s][m]));
+          }
+        }
+        SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, j, kTrVtEnd);
+      };
+      int64_t b = 0;
+      for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
         for (bool more = true; more && !*abort; ++b) {
           const int r = static_cast<int>(b % kRing);
           const int s = static_cast<int>(b & 1);
           wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
           more = (ring[r].flags & kLastBlock) == 0;
-          mbar_arrive(smem_u32(&bar_ring_empty[r]));
-          // S buffer s was last read by the softmax of block b-2
-          if (b >= 2) wait_or_flag(smem_u32(&bar_p_full[s]), ((b - 2) >> 1) & 1, abort, lim);
-          const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
-          // S = QK^T group by group, as the column groups of the stage land
+          const int4 rr = *reinterpret_cast<const int4*>(&ring[r].rows[4 * grp]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_ring_empty[r]));
 #pragma unroll
           for (int g = 0; g < kGroups; ++g) {
-            wait_or_flag(smem_u32(&bar_kv_full[s][g]), (b >> 1) & 1, abort, lim);
+            const int c0 = 2 * g;
+            const int nch = (g == kGroups - 1) ? kChunks - c0 : 2;
+            // a V^T warp copies block b-1 between its gathers of groups 0-1 and 2-3 of block b:
+            // groups 2-3 wait for PV(b-2), which the copy does not need
+            if (vt_warp && g == 2 && b >= 1) copy_vt(b - 1);
+            if (b >= 2) wait_or_flag(smem_u32(&bar_kv_empty[s][g]), ((b >> 1) - 1) & 1, abort, lim);
+            if (leader) {
+              if (g == 0) SMLA_TRACE_EVENT(b, kTrGatherIssue);
+              mbar_arrive_expect_tx(smem_u32(&bar_kv_full[s][g]), nch * 8192u);
+            }
+            if (it < 16 * nch) {
+              const int chunk = c0 + (it >> 4);
+              tma_gather4(smem_u32(sKV + s * kTileBytes + chunk * 8192 + grp * 512), &kv_map, 64 * chunk,
+                          rr.x, rr.y, rr.z, rr.w, smem_u32(&bar_kv_full[s][g]));
+            }
+          }
+        }
+      }
+      // the V^T copy of the last block
+      if (vt_warp && b >= 1 && !*abort) copy_vt(b - 1);
+      // drain: the last fills of both stages have landed before this CTA may exit
+      if (leader) {
+        for (int64_t bb = (b >= 2 ? b - 2 : 0); bb < b; ++bb)
+          for (int g = 0; g < kGroups; ++g)
+            wait_drain(smem_u32(&bar_kv_full[bb & 1][g]), (bb >> 1) & 1, lim);
+      }
+    } else if (warp == kQkWarp) {
+      // ======================================================== QK issuer (and Q tile loads)
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = make_idesc_bf16(64, kBlockN, false, false);
+        const uint64_t qd0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint32_t kv_base = smem_u32(sKV);
+        auto load_q = [&](int64_t i) {
+          const int64_t item = item_of_unit(blockIdx.x + i * gridDim.x);
+          const int64_t t = item / p.n_groups;
+          const int g = static_cast<int>(item % p.n_groups);
+          mbar_arrive_expect_tx(smem_u32(&bar_q_full), kTileBytes);
+          const int qrow = static_cast<int>(t * p.h_q + g * kGroupHeads);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, qrow, smem_u32(&bar_q_full));
+        };
+        int64_t q_loaded = 0;                      // Q tiles requested so far
+        if (n_my_items > 0) {
+          load_q(0);
+          q_loaded = 1;
+        }
+        int64_t b = 0;
+        for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
+          wait_or_flag(smem_u32(&bar_q_full), i & 1, abort, lim);
+          for (bool more = true; more && !*abort; ++b) {
+            const int r = static_cast<int>(b % kRing);
+            const int s = static_cast<int>(b & 1);
+            wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
+            more = (ring[r].flags & kLastBlock) == 0;
+            mbar_arrive(smem_u32(&bar_ring_empty[r]));
+            // S buffer s was last read by the softmax of block b-2
+            if (b >= 2) wait_or_flag(smem_u32(&bar_p_full[s]), ((b - 2) >> 1) & 1, abort, lim);
+            const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
+            // S = QK^T group by group, as the column groups of the stage land
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) {
+              wait_or_flag(smem_u32(&bar_kv_full[s][g]), (b >> 1) & 1, abort, lim);
+              tc_fence_after();
+              if (g == 0) SMLA_TRACE_EVENT(b, kTrQkIssue);
+              const int ks_end = (g == kGroups - 1) ? kQkSteps : 8 * (g + 1);
+#pragma unroll
+              for (int ks = 8 * g; ks < ks_end; ++ks) {
+                const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+                umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
+              }
+              // with V^T in TMEM, PV does not read groups 0-1 of the stage: S = QK^T releases them
+              if (kVT && g < 2) umma_commit(smem_u32(&bar_kv_empty[s][g]));
+            }
+            umma_commit(smem_u32(&bar_s_full[s]));
+            SMLA_TRACE_EVENT(b, kTrSLoaded);
+          }
+          // the next item's Q tile replaces this one once this item's last S = QK^T is done
+          if (i + 1 < n_my_items && !*abort) {
+            umma_commit(smem_u32(&bar_q_empty));
+            wait_or_flag(smem_u32(&bar_q_empty), i & 1, abort, lim);
+            load_q(i + 1);
+            ++q_loaded;
+          }
+        }
+        // drain: every MMA issued above completes before TMEM is released, and the last Q tile
+        // requested has landed before the CTA may exit
+        umma_commit(smem_u32(&bar_final_qk));
+        wait_drain(smem_u32(&bar_final_qk), 0, lim);
+        if (q_loaded > 0) wait_drain(smem_u32(&bar_q_full), (q_loaded - 1) & 1, lim);
+      }
+      __syncwarp();
+    } else if (warp == kPvWarp) {
+      // ======================================================== PV issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_pv = make_idesc_bf16(128, kGroupHeads, true, false);
+        constexpr uint32_t idesc_pv_ts = make_idesc_bf16(128, kGroupHeads, false, false);
+        const uint32_t kv_base = smem_u32(sKV);
+        int64_t b = 0;
+        for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
+          for (bool more = true; more && !*abort; ++b) {
+            const int r = static_cast<int>(b % kRing);
+            const int sb = static_cast<int>(b & 1);
+            wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
+            const uint32_t fl = ring[r].flags;
+            mbar_arrive(smem_u32(&bar_ring_empty[r]));
+            more = (fl & kLastBlock) == 0;
+            const bool first = (fl & kFirstBlock) != 0;
+            wait_or_flag(smem_u32(&bar_p_full[sb]), (b >> 1) & 1, abort, lim);
+            // the epilogue of the previous item has read all of O^T
+            if (first && i > 0) wait_or_flag(smem_u32(&bar_o_free), (i - 1) & 1, abort, lim);
             tc_fence_after();
-            if (g == 0) SMLA_TRACE_EVENT(b, kTrQkIssue);
-            const int ks_end = (g == kGroups - 1) ? kQkSteps : 8 * (g + 1);
+            SMLA_TRACE_EVENT(b, kTrPvIssue);
+            // descriptor start addresses advance in 16-byte units (low 14 bits)
+            const uint64_t b0 = make_sdesc_sw128(smem_u32(p_addr(static_cast<int>(b))), 16, 1024);
+            if constexpr (kVT) {
+              // M-chunks 2-3 from the stage first (that frees its column groups 2-3), then 0-1
+              // from V^T buffer b&1 in TMEM
+              const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
 #pragma unroll
-            for (int ks = 8 * g; ks < ks_end; ++ks) {
-              const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-              umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
+              for (int m = 2; m < 4; ++m) {
+#pragma unroll
+                for (int ks = 0; ks < kBlockN / 16; ++ks)
+                  umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
+                          b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&bar_kv_empty[sb][m]));
+              }
+#pragma unroll
+              for (int m = 0; m < 2; ++m) {
+                wait_or_flag(smem_u32(&bar_vt_full[sb][m]), (b >> 1) & 1, abort, lim);
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kBlockN / 16; ++ks)
+                  umma_ts(tmem + kTmemO + 64 * m, tmem + kTmemVT + 64 * sb + 32 * m + 8 * ks,
+                          b0 + ((ks * 32) >> 4), idesc_pv_ts, (!first || ks > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&bar_vt_free[sb][m]));   // V^T buffer sb, chunk m reusable
+              }
+            } else {
+              const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                for (int ks = 0; ks < kBlockN / 16; ++ks) {
+                  umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
+                          b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
+                }
+                // column group m of this stage has been read by every MMA that needs it (the
+                // last group's commit also covers P^T in the rope chunk)
+                umma_commit(smem_u32(&bar_kv_empty[sb][m]));
+              }
             }
+            umma_commit(smem_u32(&bar_o_done[sb]));
+            SMLA_TRACE_EVENT(b, kTrSent);
           }
-          umma_commit(smem_u32(&bar_s_full[s]));
-          SMLA_TRACE_EVENT(b, kTrSLoaded);
         }
-        // the next item's Q tile replaces this one once this item's last S = QK^T is done
-        if (i + 1 < n_my_items && !*abort) {
-          umma_commit(smem_u32(&bar_q_empty));
-          wait_or_flag(smem_u32(&bar_q_empty), i & 1, abort, lim);
-          load_q(i + 1);
-          ++q_loaded;
-        }
+        umma_commit(smem_u32(&bar_final_pv));
+        wait_drain(smem_u32(&bar_final_pv), 0, lim);
       }
-      // drain: every MMA issued above completes before TMEM is released, and the last Q tile
-      // requested has landed before the CTA may exit
-      umma_commit(smem_u32(&bar_final_qk));
-      wait_drain(smem_u32(&bar_final_qk), 0, lim);
-      if (q_loaded > 0) wait_drain(smem_u32(&bar_q_full), (q_loaded - 1) & 1, lim);
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp == kPvWarp) {
-    // ======================================================== PV issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_pv = make_idesc_bf16(128, kGroupHeads, true, false);
-      const uint32_t kv_base = smem_u32(sKV);
-      int64_t b = 0;
-      for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-        for (bool more = true; more && !*abort; ++b) {
-          const int r = static_cast<int>(b % kRing);
-          const int sb = static_cast<int>(b & 1);
-          wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
-          const uint32_t fl = ring[r].flags;
-          mbar_arrive(smem_u32(&bar_ring_empty[r]));
-          more = (fl & kLastBlock) == 0;
-          const bool first = (fl & kFirstBlock) != 0;
-          wait_or_flag(smem_u32(&bar_p_full[sb]), (b >> 1) & 1, abort, lim);
-          // the epilogue of the previous item has read all of O^T
-          if (first && i > 0) wait_or_flag(smem_u32(&bar_o_free), (i - 1) & 1, abort, lim);
-          tc_fence_after();
-          SMLA_TRACE_EVENT(b, kTrPvIssue);
-          // descriptor start addresses advance in 16-byte units (low 14 bits)
-          const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
-          const uint64_t b0 = make_sdesc_sw128(smem_u32(p_addr(static_cast<int>(b))), 16, 1024);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-#pragma unroll
-            for (int ks = 0; ks < kBlockN / 16; ++ks) {
-              umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
-                      b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
-            }
-            // column group m of this stage has been read by every MMA that needs it (the last
-            // group's commit also covers P^T in the rope chunk)
-            umma_commit(smem_u32(&bar_kv_empty[sb][m]));
-          }
-          umma_commit(smem_u32(&bar_o_done[sb]));
-          SMLA_TRACE_EVENT(b, kTrSent);
-        }
-      }
-      umma_commit(smem_u32(&bar_final_pv));
-      wait_drain(smem_u32(&bar_final_pv), 0, lim);
-    }
-    __syncwarp();
   }
 
   // ---- teardown: every tcgen05 op has completed (each item's epilogue waited on its last PV
@@ -944,7 +1065,7 @@ smla_status launch_one(const CUtensorMap& qm, const CUtensorMap& kvm, const FwdP
   // assigned round-robin
   const int64_t units = SPLIT ? p.n_items * p.n_split : p.n_items;
   const int64_t grid = units < sms ? units : sms;
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(qm, kvm, p);
+  kern<<<static_cast<unsigned>(grid), threads_for<D_QK>(), smem, stream>>>(qm, kvm, p);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_LAUNCH;
   if constexpr (SPLIT) {
     splitkv_merge_kernel<<<dim3(static_cast<unsigned>(p.n_items), kGroupHeads / kMergeHeads), kMergeThreads, 0,
