@@ -1,12 +1,13 @@
-"""CPU fp64 oracle for the sparse MLA attention forward (DSA top-k).
+"""CPU fp64 oracle for the sparse MLA attention forward and backward (DSA top-k).
 
 TEST INFRASTRUCTURE ONLY.  This package is the reference the CUDA path is checked against.
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
 import it; the product package never does, and it shares no code with the CUDA path.
 
-The arithmetic lives in ``sparse_mla_oracle.c`` (plain C, IEEE double, no fast-math), which
-states the definition it follows and cites the passages of the FlashMLA pull requests that fix
-each part.  This module only builds that file with gcc and marshals numpy arrays into it.
+The arithmetic lives in ``sparse_mla_oracle.c`` (forward) and ``sparse_mla_bwd_oracle.c``
+(backward: the gradients of sum(dO * O)), plain C in IEEE double without fast-math; each states
+the definition it follows and cites the passages of the FlashMLA pull requests that fix each
+part.  This module only builds those files with gcc and marshals numpy arrays into them.
 
 Inputs are passed exactly as the GPU receives them: q / kv as bf16 bit patterns (uint16),
 indices / topk_length as int32, attn_sink as float32, sm_scale as the float32 value.
@@ -24,20 +25,28 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "sparse_mla_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libsmla_oracle.so")
+_BWD_SRC = os.path.join(_HERE, "sparse_mla_bwd_oracle.c")
+_BWD_LIB_PATH = os.path.join(_BUILD_DIR, "libsmla_bwd_oracle.so")
 _lock = threading.Lock()
 _lib = None
+_bwd_lib = None
+
+
+def _compile(src, lib_path, force):
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(lib_path)) or os.path.getmtime(lib_path) < os.path.getmtime(src)
+    if force or stale:
+        tmp = lib_path + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-shared", "-fPIC", "-o", tmp, src, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle shared library (gcc, -O2, OpenMP).  Returns its path."""
-    os.makedirs(_BUILD_DIR, exist_ok=True)
-    stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
-    if force or stale:
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    """Compile the oracle shared libraries (gcc, -O2, OpenMP).  Returns the forward's path."""
+    _compile(_BWD_SRC, _BWD_LIB_PATH, force)
+    return _compile(_SRC, _LIB_PATH, force)
 
 
 def _bind(lib):
@@ -159,3 +168,84 @@ class Variant:
 
     def last_valid_length(self, *a, **kw):
         return last_valid_length(*a, _lib_=self._lib, **kw)
+
+
+# ---------------------------------------------------------------------------------- backward
+def _bind_bwd(lib):
+    P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    lib.smla_oracle_bwd.restype = ctypes.c_int
+    lib.smla_oracle_bwd.argtypes = [P, P, P, P, P, P, D, I64, I64, I32, I32, I32, I32, P, P, P, I32]
+    return lib
+
+
+def _load_bwd():
+    global _bwd_lib
+    with _lock:
+        if _bwd_lib is None:
+            build()
+            _bwd_lib = _bind_bwd(ctypes.CDLL(_BWD_LIB_PATH))
+    return _bwd_lib
+
+
+def bf16_bits_to_f64(bits):
+    """bf16 bit patterns (uint16) -> float64, exactly."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def sparse_mla_bwd_f64(q, kv, dout, indices, topk_length=None, attn_sink=None, sm_scale=None,
+                       threads=0, _lib_=None):
+    """fp64 gradients of sum(dout * O) for real-valued inputs.  q [s_q, h_q, d_qk],
+    kv [s_kv, d_qk] (or [s_kv, 1, d_qk]), dout [s_q, h_q, d_v] float64; indices [s_q, topk]
+    (or [s_q, 1, topk]) int32.  Returns (dq [s_q, h_q, d_qk], dkv [s_kv, d_qk], dsink [h_q] or
+    None) as float64."""
+    lib = _lib_ or _load_bwd()
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    dout = np.ascontiguousarray(dout, dtype=np.float64)
+    s_q, h_q, d_qk = q.shape
+    kv = np.ascontiguousarray(kv, dtype=np.float64).reshape(-1, d_qk)
+    s_kv = kv.shape[0]
+    d_v = dout.shape[2]
+    indices = _c(indices, np.int32).reshape(s_q, -1)
+    topk = indices.shape[1]
+    if sm_scale is None:
+        sm_scale = float(np.float32(1.0 / np.sqrt(d_qk)))
+    dq = np.empty((s_q, h_q, d_qk), np.float64)
+    dkv = np.empty((s_kv, d_qk), np.float64)
+    sink = _c(attn_sink, np.float32)
+    dsink = np.empty(h_q, np.float64) if sink is not None else None
+    tl = _c(topk_length, np.int32)
+    rc = lib.smla_oracle_bwd(_ptr(q), _ptr(kv), _ptr(dout), _ptr(indices), _ptr(tl), _ptr(sink),
+                             float(sm_scale), s_q, s_kv, h_q, d_qk, d_v, topk, _ptr(dq), _ptr(dkv),
+                             _ptr(dsink), int(threads))
+    if rc != 0:
+        raise ValueError("backward oracle ran out of memory")
+    return dq, dkv, dsink
+
+
+def sparse_mla_bwd(q_bits, kv_bits, dout_bits, indices, topk_length=None, attn_sink=None,
+                   sm_scale=None, threads=0, _lib_=None):
+    """fp64 gradients of sum(dout * O) for bf16 inputs given as bit patterns (uint16), exactly as
+    the GPU receives them.  Same outputs as :func:`sparse_mla_bwd_f64`."""
+    return _bwd_f64(bf16_bits_to_f64(q_bits), bf16_bits_to_f64(kv_bits),
+                    bf16_bits_to_f64(dout_bits), indices, topk_length, attn_sink, sm_scale,
+                    threads, _lib_=_lib_)
+
+
+# fixed references for BwdVariant (the pin tests rebind the public names to a variant)
+_bwd_f64 = sparse_mla_bwd_f64
+_bwd_bits = sparse_mla_bwd
+
+
+class BwdVariant:
+    """The backward bound to another build of its source (a shared library at ``path``); the
+    pin tests use it to check that planted mistakes are caught."""
+
+    def __init__(self, path):
+        self._lib = _bind_bwd(ctypes.CDLL(path))
+
+    def sparse_mla_bwd_f64(self, *a, **kw):
+        return _bwd_f64(*a, _lib_=self._lib, **kw)
+
+    def sparse_mla_bwd(self, *a, **kw):
+        return _bwd_bits(*a, _lib_=self._lib, **kw)
