@@ -1,5 +1,6 @@
 /*
- * sparse_mla.h -- C ABI of the GB300 (sm_103a) sparse MLA attention forward (DSA top-k).
+ * sparse_mla.h -- C ABI of the GB300 (sm_103a) sparse MLA attention forward (DSA top-k) and
+ * its backward.
  *
  * The operation (FlashMLA PR #196, "Problem" and "Fix"; FlashMLA PR #216, "Summary";
  * FlashMLA PR #198, "Summary" item 2):
@@ -38,7 +39,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 2
+#define SMLA_ABI_VERSION 3
 
 typedef struct CUstream_st* smla_stream_t; /* a cudaStream_t; NULL = legacy default stream */
 
@@ -170,6 +171,39 @@ smla_status sparse_mla_device_status(int reset);
  * sparse_mla_device_status after synchronising.  SMLA_ERR_BAD_SHAPE for a limit out of range.
  */
 smla_status sparse_mla_selftest_wait_timeout(uint64_t limit_ns, smla_stream_t stream);
+
+/*
+ * Sparse MLA backward over one shared latent KV (FlashMLA PR #198, "Summary" item 1: the
+ * sparse MLA backward, dK / dV scattered into the shared latent rows).  It returns the
+ * gradients of  L = sum_{t,h,d} dout[t,h,d] * O[t,h,d]  for the forward above:
+ *   p_j      = exp(sm_scale <q[t,h,:], K[idx_j]> - lse_full[t,h]),
+ *              lse_full = ln(exp(lse[t,h]) + [attn_sink] exp(attn_sink[h]))
+ *   D[t,h]   = <dout[t,h,:], out[t,h,:]>,   dS_j = p_j (<dout[t,h,:], V[idx_j]> - D[t,h])
+ *   dq[t,h,:]            = sm_scale sum_j dS_j K[idx_j]
+ *   dkv[idx_j, :d_qk]   += sm_scale dS_j q[t,h,:]     (summed over every row, head and slot)
+ *   dkv[idx_j, :d_v]    += p_j dout[t,h,:]
+ *   dsink[h]            += -exp(attn_sink[h] - lse_full[t,h]) D[t,h]
+ * over the same counted slots as the forward (j < L_t and 0 <= idx < s_kv; duplicated indices
+ * count once per slot).  A row without a counted slot contributes nothing (its dq is 0).
+ *   q, kv, indices, topk_length, attn_sink, sm_scale, d_v: as for sparse_mla_fwd
+ *   out          [s_q, h_q, d_v]   bf16   the forward's output (16-byte aligned)
+ *   dout         [s_q, h_q, d_v]   bf16   gradient of the loss w.r.t. out (16-byte aligned)
+ *   lse          [s_q, h_q]        fp32   the forward's lse (natural log, sink excluded)
+ *   dq           [s_q, h_q, d_qk]  fp32   (written)
+ *   dkv          [s_kv, d_qk]      fp32   (written: zeroed on the stream, then accumulated
+ *                                          with fp32 atomics, so the summation order and the
+ *                                          last bits vary from run to run); may be NULL only
+ *                                          when s_kv == 0
+ *   dsink        [h_q]             fp32 or NULL (written when attn_sink is given: zeroed,
+ *                                          then accumulated; zeroed otherwise)
+ * Every row's work is bounded by L_t (topk_length, or topk); slots in [0, L_t) that do not
+ * count are masked.  Uses no workspace and allocates nothing.  With s_q == 0, dkv and dsink
+ * are zeroed and nothing else happens.
+ */
+smla_status sparse_mla_bwd(const void* q, const void* kv, const void* out, const void* dout,
+                           const int32_t* indices, const int32_t* topk_length, const float* attn_sink,
+                           const float* lse, float sm_scale, int d_v, float* dq, float* dkv, float* dsink,
+                           int64_t s_q, int64_t s_kv, int h_q, int d_qk, int topk, smla_stream_t stream);
 
 /* Static, human-readable description of a status code.  Never NULL. */
 const char* sparse_mla_status_string(smla_status status);

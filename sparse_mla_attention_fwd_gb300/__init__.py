@@ -1,4 +1,4 @@
-"""GB300-native sparse MLA attention forward (DeepSeek-style DSA top-k), sm_103a.
+"""GB300-native sparse MLA attention forward and backward (DeepSeek-style DSA top-k), sm_103a.
 
 Python names mirror the C ABI of include/sparse_mla.h.  Tensors are torch CUDA tensors (torch
 supplies device memory and streams only); outputs are allocated here when not given.
@@ -11,6 +11,10 @@ query row attends to the slots j < L_t of its index list whose index lies in [0,
 topk_length[t] clamped to [0, topk] when given, else topk.  O is bf16; lse (natural log, sink
 excluded) and max_logits (max of sm_scale * q.k) are fp32; a row without a counted slot gives
 O = 0, lse = +inf, max_logits = -inf.
+
+    dq, dkv, dsink = sparse_mla_bwd(q, kv, out, dout, indices, lse, topk_length, attn_sink)
+
+returns the gradients of sum(dout * out) (FlashMLA PR #198, "Summary" item 1) in fp32.
 """
 from __future__ import annotations
 
@@ -22,7 +26,7 @@ from ._native import EXPORTED, SmlaError, load_library, status_string
 from .native_build import LIB_PATH, build as build_library
 
 __all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_fwd_paged_splitkv_static", "auto_splits",
-           "sparse_mla_device_status",
+           "sparse_mla_bwd", "sparse_mla_device_status",
            "sparse_mla_status_string", "SmlaError", "load_library", "build_library", "LIB_PATH"]
 
 
@@ -222,6 +226,56 @@ def sparse_mla_fwd_paged_splitkv_static(q, kv_pool, block_table, indices, n_spli
     if rc != 0:
         raise SmlaError(rc, "sparse_mla_fwd_paged_splitkv_static")
     return out, lse, max_logits
+
+
+def sparse_mla_bwd(q, kv, out, dout, indices, lse, topk_length=None, attn_sink=None, sm_scale=None,
+                   d_v=512, dq=None, dkv=None, dsink=None, stream=None):
+    """Gradients of sum(dout * out) through the forward: q, kv, indices, topk_length, attn_sink and
+    sm_scale as passed to :func:`sparse_mla_fwd`; out [s_q, h_q, d_v] bf16 and lse [s_q, h_q]
+    fp32 as it returned them; dout [s_q, h_q, d_v] bf16.  Returns (dq [s_q, h_q, d_qk] fp32,
+    dkv [s_kv, d_qk] fp32, dsink [h_q] fp32 or None)."""
+    lib = load_library()
+    _check(q, "q", torch.bfloat16)
+    dev = q.device
+    _check(kv, "kv", torch.bfloat16, dev)
+    _check(out, "out", torch.bfloat16, dev)
+    _check(dout, "dout", torch.bfloat16, dev)
+    _check(indices, "indices", torch.int32, dev)
+    _check(lse, "lse", torch.float32, dev)
+    _check(topk_length, "topk_length", torch.int32, dev)
+    _check(attn_sink, "attn_sink", torch.float32, dev)
+    s_q, h_q, d_qk = q.shape
+    s_kv = kv.shape[0]
+    if kv.numel() != s_kv * d_qk:
+        raise ValueError("kv must be [s_kv, 1, d_qk] with the d_qk of q")
+    topk = indices.shape[-1] if indices.dim() else 0
+    if indices.numel() != s_q * topk:
+        raise ValueError("indices must be [s_q, 1, topk]")
+    if out.numel() != s_q * h_q * d_v or dout.numel() != s_q * h_q * d_v or lse.numel() != s_q * h_q:
+        raise ValueError("out / dout must be [s_q, h_q, d_v] and lse [s_q, h_q]")
+    if topk_length is not None and topk_length.numel() != s_q:
+        raise ValueError("topk_length must have s_q entries")
+    if attn_sink is not None and attn_sink.numel() != h_q:
+        raise ValueError("attn_sink must have h_q entries")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d_qk)
+    if dq is None:
+        dq = torch.empty((s_q, h_q, d_qk), dtype=torch.float32, device=dev)
+    if dkv is None:
+        dkv = torch.empty((s_kv, d_qk), dtype=torch.float32, device=dev)
+    if dsink is None and attn_sink is not None:
+        dsink = torch.empty((h_q,), dtype=torch.float32, device=dev)
+    _check(dq, "dq", torch.float32, dev)
+    _check(dkv, "dkv", torch.float32, dev)
+    _check(dsink, "dsink", torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib.sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(out), _ptr(dout), _ptr(indices), _ptr(topk_length),
+                                _ptr(attn_sink), _ptr(lse), float(sm_scale), int(d_v), _ptr(dq), _ptr(dkv),
+                                _ptr(dsink), int(s_q), int(s_kv), int(h_q), int(d_qk), int(topk),
+                                _stream_handle(stream, dev))
+    if rc != 0:
+        raise SmlaError(rc, "sparse_mla_bwd")
+    return dq, dkv, dsink
 
 
 def sparse_mla_device_status(reset=False) -> int:

@@ -18,7 +18,7 @@ STATUS_NAMES = {0: "SMLA_OK", 1: "SMLA_ERR_NULL_PTR", 2: "SMLA_ERR_BAD_SHAPE",
 EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_splitkv_workspace_size",
             "sparse_mla_fwd_splitkv", "sparse_mla_fwd_paged_splitkv", "sparse_mla_fwd_paged_splitkv_static",
             "sparse_mla_selftest_wait_timeout", "sparse_mla_device_status",
-            "sparse_mla_status_string", "sparse_mla_abi_version")
+            "sparse_mla_status_string", "sparse_mla_abi_version", "sparse_mla_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +68,8 @@ def load_library(path: str | None = None):
         lib.sparse_mla_status_string.argtypes = [I32]
         lib.sparse_mla_abi_version.restype = I32
         lib.sparse_mla_abi_version.argtypes = []
+        lib.sparse_mla_bwd.restype = I32
+        lib.sparse_mla_bwd.argtypes = [P, P, P, P, P, P, P, P, F32, I32, P, P, P, I64, I64, I32, I32, I32, P]
         _lib = lib
         return lib
 

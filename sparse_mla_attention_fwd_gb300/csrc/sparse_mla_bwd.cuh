@@ -1,0 +1,462 @@
+// Sparse MLA attention backward (DSA top-k) for sm_103a.  Included by sparse_mla_fwd.cu inside
+// namespace smla::(anonymous): it shares that file's bounded waits, status word, tensor-map
+// encoding and argument checks.
+//
+// The operation (FlashMLA PR #198, "Summary" item 1: the sparse MLA backward for the absorbed
+// shape, dK / dV scattered into the shared latent rows with fp32 atomics): the gradients of
+// L = sum dO * O through the forward of PR #196 / #216 / #198 item 2.  For row t, head h and the
+// counted slots s (latent row r_s, key k_s = kv[r_s, :d_qk], value v_s = kv[r_s, :d_v]):
+//   p_s  = exp(sm_scale q.k_s - lse_full),   lse_full = ln(exp(lse) + [sink] exp(sink_h))
+//   D    = <dO, O>,   dS_s = p_s (<dO, v_s> - D)
+//   dq_h += sm_scale dS_s k_s,   dkv[r_s, :d_qk] += sm_scale dS_s q_h,   dkv[r_s, :d_v] += p_s dO_h
+//   dsink[h] += -exp(sink_h - lse_full) D
+// lse is the forward's (natural log, sink excluded) and O the forward's bf16 output.
+//
+// Work item = (token, group of 64 heads), one CTA each.  Per 64-key block of the row:
+//   S   [64 heads x 64 keys] = Q K^T              (M=64, N=64, K=d_qk; TMEM)
+//   dP  [64 heads x 64 keys] = dO V^T             (M=64, N=64, K=512; TMEM)
+//   P, dS' = sm_scale P (dP - D)  -> shared memory as bf16 [heads][keys] (SW128)
+//   dQ^T [d_qk x 64 heads] += K^T dS'^T           (M=128 (+64 for the rope), N=64, K=64 keys;
+//                                                  TMEM, accumulated over the row's blocks)
+//   dKV^T [d x 64 keys]     = Q^T dS' + dO^T P    (per 128-row chunk of d, K=64 heads; TMEM),
+//                             drained by the math warps into fp32 reductions on dkv
+// Warp roles (384 threads): warp 0 issues every MMA (one thread) and owns TMEM; warps 1-3 and
+// 8-11 gather the block's kv rows with TMA gather4 (warp 1 also loads the Q and dO tiles);
+// warps 4-7 (TMEM lane quadrants 0-3) compute P / dS', drain dKV^T and write dq.
+// TMEM: dQ^T chunks at columns 0, 64, 128, 192 (+256 for the rope rows), S at 320, dP at 384,
+// and three 64-column dKV^T buffers at 448, 320 and 384 (the last two reuse S and dP once the
+// math warps have read them).
+
+constexpr int kBwdThreads = 384;
+constexpr int kBwdMathWarp0 = 4;
+constexpr int kBwdGatherWarps = 7;                 // warps 1, 2, 3, 8, 9, 10, 11
+constexpr uint32_t kBwdTmemS = 320, kBwdTmemDP = 384, kBwdTmemX0 = 448;
+
+struct BwdParams {
+  const int32_t* indices;      // [s_q, topk]
+  const int32_t* topk_length;  // [s_q] or null
+  const float* attn_sink;      // [h_q] or null
+  const float* lse;            // [s_q, h_q], natural log, sink excluded
+  const __nv_bfloat16* out;    // [s_q, h_q, 512]
+  const __nv_bfloat16* dout;   // [s_q, h_q, 512]
+  float* dq;                   // [s_q, h_q, d_qk]
+  float* dkv;                  // [s_kv, d_qk], accumulated
+  float* dsink;                // [h_q] or null, accumulated
+  float sm_scale;
+  int64_t s_q;
+  int64_t s_kv;
+  int h_q;
+  int topk;
+  int n_groups;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ uint32_t bwd_dkv_col(int c) {
+  const int i = c % 3;
+  return i == 0 ? kBwdTmemX0 : (i == 1 ? kBwdTmemS : kBwdTmemDP);
+}
+
+// TMA row coordinate of slot j of row t (j < L): the kv row, or -1 when the slot does not count
+__device__ __forceinline__ int bwd_row(const BwdParams& p, const int32_t* idx_row, int j, int L) {
+  if (j >= L) return -1;
+  const int v = __ldg(idx_row + j);
+  return (v >= 0 && static_cast<int64_t>(v) < p.s_kv) ? v : -1;
+}
+
+template <int D_QK>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    sparse_mla_bwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap do_map,
+                          const __grid_constant__ CUtensorMap kv_map, const BwdParams p) {
+  constexpr int kChunks = D_QK / 64;                 // 64-column chunks of q / kv rows
+  constexpr int kQkSteps = D_QK / 16;
+  constexpr int kDkvChunks = (D_QK + 127) / 128;     // 128-row chunks of d (the last may be 64)
+  constexpr bool kRope = (D_QK % 128) != 0;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;                                 // [64 heads][D_QK], kChunks x 8 KB
+  uint8_t* sDO = sQ + kChunks * 8192;                 // [64 heads][512], 8 x 8 KB
+  uint8_t* sKV = sDO + 8 * 8192;                      // [64 keys][D_QK], kChunks x 8 KB
+  uint8_t* sP = sKV + kChunks * 8192;                 // [64 heads][64 keys] bf16
+  uint8_t* sDS = sP + 8192;                           // [64 heads][64 keys] bf16 (sm_scale dS)
+
+  __shared__ __align__(8) uint64_t bar_qdo_full, bar_kv_full, bar_kv_empty, bar_s_full, bar_p_full,
+      bar_tiles_free, bar_dq_full, bar_final;
+  __shared__ __align__(8) uint64_t bar_x_full[3], bar_x_free[3];
+  __shared__ int32_t s_rows[2][64];
+  __shared__ float s_delta[64];
+  __shared__ float s_lse2[64];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  volatile int* abort = &abort_flag;
+  const uint64_t lim = p.wait_limit_ns;
+  const int64_t item = blockIdx.x;
+  const int64_t t = item / p.n_groups;
+  const int g = static_cast<int>(item % p.n_groups);
+  const int32_t* idx_row = p.indices + t * static_cast<int64_t>(p.topk);
+  const int L = p.topk_length ? min(max(__ldg(p.topk_length + t), 0), p.topk) : p.topk;
+  const int nb = (L + 63) / 64;                       // blocks of this row (uniform for all roles)
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_qdo_full), 1);
+    mbar_init(smem_u32(&bar_kv_full), 1);
+    mbar_init(smem_u32(&bar_kv_empty), 1);
+    mbar_init(smem_u32(&bar_s_full), 1);
+    mbar_init(smem_u32(&bar_p_full), 128);
+    mbar_init(smem_u32(&bar_tiles_free), 1);
+    mbar_init(smem_u32(&bar_dq_full), 1);
+    mbar_init(smem_u32(&bar_final), 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(smem_u32(&bar_x_full[i]), 1);
+      mbar_init(smem_u32(&bar_x_free[i]), 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int64_t qrow = t * p.h_q + static_cast<int64_t>(g) * 64;   // first (token, head) row
+
+  if (warp == 0) {
+    // ======================================================== MMA issuer
+    if (lane == 0 && nb > 0) {
+      constexpr uint32_t id_s = make_idesc_bf16(64, 64, false, false);
+      constexpr uint32_t id_dq = make_idesc_bf16(128, 64, true, false);
+      constexpr uint32_t id_dq64 = make_idesc_bf16(64, 64, true, false);
+      constexpr uint32_t id_kv = make_idesc_bf16(128, 64, true, true);
+      constexpr uint32_t id_kv64 = make_idesc_bf16(64, 64, true, true);
+      const uint64_t q_k = make_sdesc_sw128(smem_u32(sQ), 16, 1024);      // Q, K-major
+      const uint64_t do_k = make_sdesc_sw128(smem_u32(sDO), 16, 1024);    // dO, K-major
+      const uint64_t kv_k = make_sdesc_sw128(smem_u32(sKV), 16, 1024);    // K / V rows, K-major
+      const uint64_t kv_mn = make_sdesc_sw128(smem_u32(sKV), 8192, 1024); // K^T, MN-major
+      const uint64_t q_mn = make_sdesc_sw128(smem_u32(sQ), 8192, 1024);   // Q^T, MN-major
+      const uint64_t do_mn = make_sdesc_sw128(smem_u32(sDO), 8192, 1024); // dO^T, MN-major
+      const uint64_t ds_k = make_sdesc_sw128(smem_u32(sDS), 16, 1024);    // dS'^T operand, K-major
+      const uint64_t ds_mn = make_sdesc_sw128(smem_u32(sDS), 8192, 1024); // dS' operand, MN-major
+      const uint64_t p_mn = make_sdesc_sw128(smem_u32(sP), 8192, 1024);   // P operand, MN-major
+      uint32_t xu[3] = {0u, 0u, 0u};                  // fills of each dKV^T buffer so far
+      wait_or_flag(smem_u32(&bar_qdo_full), 0, abort, lim);
+      for (int b = 0; b < nb && !*abort; ++b) {
+        wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);
+        // S and dP reuse the columns of dKV^T buffers 1 and 2: every drain of them is done
+        if (xu[1] > 0) wait_or_flag(smem_u32(&bar_x_free[1]), (xu[1] - 1) & 1, abort, lim);
+        if (xu[2] > 0) wait_or_flag(smem_u32(&bar_x_free[2]), (xu[2] - 1) & 1, abort, lim);
+        tc_fence_after();
+#pragma unroll 4
+        for (int ks = 0; ks < kQkSteps; ++ks) {
+          const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+          umma_ss(tmem + kBwdTmemS, q_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
+        }
+#pragma unroll 4
+        for (int ks = 0; ks < 32; ++ks) {
+          const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+          umma_ss(tmem + kBwdTmemDP, do_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&bar_s_full));
+        wait_or_flag(smem_u32(&bar_p_full), b & 1, abort, lim);
+        tc_fence_after();
+        // dQ^T += K^T dS'^T over this block's 64 keys
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_ss(tmem + 64 * c, kv_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_dq,
+                    (b > 0 || ks > 0) ? 1u : 0u);
+        if constexpr (kRope) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_ss(tmem + 256, kv_mn + ((8 * 8192 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_dq64,
+                    (b > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&bar_kv_empty));          // S, dP and dQ^T have read the stage
+        // dKV^T chunk c = Q^T dS' (+ dO^T P on the value rows), one buffer of three each
+#pragma unroll
+        for (int c = 0; c < kDkvChunks; ++c) {
+          const int i = c % 3;
+          if (xu[i] > 0) wait_or_flag(smem_u32(&bar_x_free[i]), (xu[i] - 1) & 1, abort, lim);
+          tc_fence_after();
+          const uint32_t col = tmem + bwd_dkv_col(c);
+          if (!kRope || c < 4) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_ss(col, q_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv,
+                      ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_ss(col, do_mn + ((2 * c * 8192 + ks * 2048) >> 4), p_mn + ((ks * 2048) >> 4), id_kv, 1u);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_ss(col, q_mn + ((8 * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv64,
+                      ks > 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&bar_x_full[i]));
+          ++xu[i];
+        }
+        umma_commit(smem_u32(&bar_tiles_free));        // P and dS' tiles may be rewritten
+      }
+      umma_commit(smem_u32(&bar_dq_full));
+      umma_commit(smem_u32(&bar_final));
+      wait_drain(smem_u32(&bar_final), 0, lim);
+    }
+    __syncwarp();
+  } else if (warp >= kBwdMathWarp0 && warp < kBwdMathWarp0 + 4) {
+    // ======================================================== P / dS', dKV^T drains, dq
+    const int q = warp - kBwdMathWarp0;
+    const int mt = tid - kBwdMathWarp0 * 32;         // 0..127
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // per-item prologue: D = <dO, O> and lse_full * log2(e) for each of the 64 heads (two
+    // threads per head, 256 columns each), and the sink's gradient
+    {
+      const int h = mt >> 1, half = mt & 1;
+      const int64_t r = (qrow + h) * 512 + half * 256;
+      const uint4* a = reinterpret_cast<const uint4*>(p.dout + r);
+      const uint4* o = reinterpret_cast<const uint4*>(p.out + r);
+      float acc = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const uint4 x = __ldg(a + k), y = __ldg(o + k);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
+          const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[e]));
+          acc = fmaf(fx.x, fy.x, acc);
+          acc = fmaf(fx.y, fy.y, acc);
+        }
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      if (half == 0) {
+        const int head = g * 64 + h;
+        const float lse = __ldg(p.lse + t * p.h_q + head);
+        float lf = lse;
+        if (p.attn_sink) {
+          const float sk = __ldg(p.attn_sink + head);
+          const float hi = fmaxf(lse, sk);
+          lf = (hi == INFINITY) ? INFINITY : hi + log1pf(expf(fminf(lse, sk) - hi));
+          if (p.dsink) atomicAdd(p.dsink + head, -expf(sk - lf) * acc);
+        }
+        s_delta[h] = acc;
+        s_lse2[h] = lf * kLog2e;
+      }
+    }
+    named_bar_sync(1, 128);
+    const int hA = 16 * q + (lane >> 2), hB = hA + 8;
+    const int cpair = 2 * (lane & 3);
+    const float c2 = p.sm_scale * kLog2e;
+    const float dA = s_delta[hA], dB = s_delta[hB];
+    const float lA = s_lse2[hA], lB = s_lse2[hB];
+    uint32_t xu[3] = {0u, 0u, 0u};
+    for (int b = 0; b < nb && !*abort; ++b) {
+      const int sb = b & 1;
+      wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);   // also publishes s_rows[sb]
+      wait_or_flag(smem_u32(&bar_s_full), b & 1, abort, lim);
+      tc_fence_after();
+      float sv[32], dv[32];
+#pragma unroll
+      for (int i8 = 0; i8 < 8; ++i8) {
+        uint32_t r4[4], d4[4];
+        tmem_ld_16x256b(tmem + lane_base + kBwdTmemS + 8 * i8, r4);
+        tmem_ld_16x256b(tmem + lane_base + kBwdTmemDP + 8 * i8, d4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sv[4 * i8 + e] = __uint_as_float(r4[e]);
+          dv[4 * i8 + e] = __uint_as_float(d4[e]);
+        }
+      }
+      tmem_ld_wait();
+      // the previous block's P / dS' tiles have been read by every MMA
+      if (b >= 1) wait_or_flag(smem_u32(&bar_tiles_free), (b - 1) & 1, abort, lim);
+      const int swA = hA & 7, swB = hB & 7;
+#pragma unroll
+      for (int i8 = 0; i8 < 8; ++i8) {
+        float pa[2], pb[2], da[2], db[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool ok = s_rows[sb][8 * i8 + cpair + e] >= 0;
+          pa[e] = ok ? fast_exp2(fmaf(sv[4 * i8 + e], c2, -lA)) : 0.f;
+          pb[e] = ok ? fast_exp2(fmaf(sv[4 * i8 + 2 + e], c2, -lB)) : 0.f;
+          da[e] = p.sm_scale * pa[e] * (dv[4 * i8 + e] - dA);
+          db[e] = p.sm_scale * pb[e] * (dv[4 * i8 + 2 + e] - dB);
+        }
+        const int off = 2 * cpair;
+        *reinterpret_cast<uint32_t*>(sP + hA * 128 + ((i8 ^ swA) << 4) + off) = pack_bf16x2(pa[0], pa[1]);
+        *reinterpret_cast<uint32_t*>(sP + hB * 128 + ((i8 ^ swB) << 4) + off) = pack_bf16x2(pb[0], pb[1]);
+        *reinterpret_cast<uint32_t*>(sDS + hA * 128 + ((i8 ^ swA) << 4) + off) = pack_bf16x2(da[0], da[1]);
+        *reinterpret_cast<uint32_t*>(sDS + hB * 128 + ((i8 ^ swB) << 4) + off) = pack_bf16x2(db[0], db[1]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p_full));
+      // drain this block's dKV^T chunks into fp32 reductions on the selected kv rows
+#pragma unroll
+      for (int c = 0; c < kDkvChunks; ++c) {
+        const int i = c % 3;
+        wait_or_flag(smem_u32(&bar_x_full[i]), xu[i] & 1, abort, lim);
+        ++xu[i];
+        tc_fence_after();
+        const bool rope = kRope && c == 4;
+        const int d = rope ? 512 + 16 * q + lane : 128 * c + 32 * q + lane;
+        float* base = p.dkv + d;
+        // two halves of 32 keys; the buffer goes back once both are in registers
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tmem_ld16(tmem + lane_base + bwd_dkv_col(c) + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+          tmem_ld16(tmem + lane_base + bwd_dkv_col(c) + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+          tmem_ld_wait();
+          if (half == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_x_free[i]));
+          }
+          if (!rope || lane < 16) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int row = s_rows[sb][32 * half + k];
+              if (row >= 0) atomicAdd(base + static_cast<int64_t>(row) * D_QK, __uint_as_float(v[k]));
+            }
+          }
+        }
+      }
+    }
+    // ---- dq of this item: dQ^T chunk c holds rows d, columns = heads
+    float* dq = p.dq + qrow * D_QK;
+    if (nb > 0) {
+      wait_or_flag(smem_u32(&bar_dq_full), 0, abort, lim);
+      tc_fence_after();
+    }
+#pragma unroll 1
+    for (int c = 0; c < kDkvChunks; ++c) {
+      const bool rope = kRope && c == 4;
+      const int d = rope ? 512 + 16 * q + lane : 128 * c + 32 * q + lane;
+#pragma unroll 1
+      for (int h16 = 0; h16 < 4; ++h16) {
+        uint32_t r[16];
+        if (nb > 0) {
+          tmem_ld16(tmem + lane_base + 64 * c + 16 * h16, r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) r[j] = 0u;
+        }
+        if (!rope || lane < 16) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dq[static_cast<int64_t>(16 * h16 + j) * D_QK + d] = __uint_as_float(r[j]);
+        }
+      }
+    }
+  } else {
+    // ======================================================== gather (warps 1-3, 8-11)
+    const int gw = warp < 4 ? warp - 1 : warp - 5;   // 0..6
+    const bool leader = (gw == 0 && lane == 0);
+    if (leader && nb > 0) {
+      mbar_arrive_expect_tx(smem_u32(&bar_qdo_full), (kChunks + 8) * 8192u);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
+      for (int c = 0; c < 8; ++c)
+        tma_load_2d(smem_u32(sDO + c * 8192), &do_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
+    }
+    const int it = gw + kBwdGatherWarps * lane;       // (4-row group, chunk) item of a block
+    const int grp = it & 15, chunk = it >> 4;
+    for (int b = 0; b < nb && !*abort; ++b) {
+      if (b >= 1) wait_or_flag(smem_u32(&bar_kv_empty), (b - 1) & 1, abort, lim);
+      if (gw == 0) {
+        s_rows[b & 1][lane] = bwd_row(p, idx_row, 64 * b + lane, L);
+        s_rows[b & 1][lane + 32] = bwd_row(p, idx_row, 64 * b + lane + 32, L);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bar_kv_full), kChunks * 8192u);
+      }
+      if (it < 16 * kChunks) {
+        const int j = 64 * b + 4 * grp;
+        tma_gather4(smem_u32(sKV + chunk * 8192 + grp * 512), &kv_map, 64 * chunk, bwd_row(p, idx_row, j, L),
+                    bwd_row(p, idx_row, j + 1, L), bwd_row(p, idx_row, j + 2, L), bwd_row(p, idx_row, j + 3, L),
+                    smem_u32(&bar_kv_full));
+      }
+    }
+    // the Q / dO tiles and the last block have landed before this CTA may exit
+    if (leader && nb > 0) {
+      wait_drain(smem_u32(&bar_qdo_full), 0, lim);
+      wait_drain(smem_u32(&bar_kv_full), (nb - 1) & 1, lim);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D_QK>
+smla_status launch_bwd(const CUtensorMap& qm, const CUtensorMap& dom, const CUtensorMap& kvm, const BwdParams& p,
+                       int64_t n_items, cudaStream_t stream) {
+  auto kern = sparse_mla_bwd_kernel<D_QK>;
+  constexpr int kChunks = D_QK / 64;
+  const size_t smem = (2 * kChunks + 10) * 8192 + 1024;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return SMLA_ERR_LAUNCH;
+  kern<<<static_cast<unsigned>(n_items), kBwdThreads, smem, stream>>>(qm, dom, kvm, p);
+  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
+}
+
+smla_status bwd_flat(const void* q, const void* kv, const void* out, const void* dout, const int32_t* indices,
+                     const int32_t* topk_length, const float* attn_sink, const float* lse, float sm_scale,
+                     int d_v, float* dq, float* dkv, float* dsink, int64_t s_q, int64_t s_kv, int h_q, int d_qk,
+                     int topk, cudaStream_t stream) {
+  // every argument is checked before anything is enqueued
+  if (s_kv < 0) return SMLA_ERR_BAD_SHAPE;
+  smla_status st = check_common(q, s_kv > 0 ? kv : q, indices, dq, lse, dq, s_q, h_q, d_qk, d_v, topk, sm_scale);
+  if (st != SMLA_OK) return st;
+  if (s_q > 0) {
+    if (!out || !dout) return SMLA_ERR_NULL_PTR;
+    if (!aligned16(out) || !aligned16(dout)) return SMLA_ERR_MISALIGNED;
+    if (attn_sink && !aligned4(attn_sink)) return SMLA_ERR_MISALIGNED;
+    if (topk_length && !aligned4(topk_length)) return SMLA_ERR_MISALIGNED;
+  }
+  if (s_kv > 0 && !dkv) return SMLA_ERR_NULL_PTR;
+  if ((dkv && !aligned4(dkv)) || (dsink && !aligned4(dsink))) return SMLA_ERR_MISALIGNED;
+  // dkv and dsink are accumulated into: they start at zero
+  if (s_kv > 0 && cudaMemsetAsync(dkv, 0, static_cast<size_t>(s_kv) * d_qk * sizeof(float), stream) != cudaSuccess)
+    return SMLA_ERR_LAUNCH;
+  if (dsink && cudaMemsetAsync(dsink, 0, static_cast<size_t>(h_q) * sizeof(float), stream) != cudaSuccess)
+    return SMLA_ERR_LAUNCH;
+  if (s_q == 0) return SMLA_OK;
+  CUtensorMap qm, dom, kvm;
+  const uint64_t rows = static_cast<uint64_t>(s_q) * h_q;
+  if (!make_map(&qm, q, rows, d_qk, 64) || !make_map(&dom, dout, rows, d_v, 64)) return SMLA_ERR_TENSOR_MAP;
+  if (!make_map(&kvm, s_kv > 0 ? kv : q, s_kv > 0 ? static_cast<uint64_t>(s_kv) : 1u, d_qk, 1))
+    return SMLA_ERR_TENSOR_MAP;
+  BwdParams p{};
+  p.indices = indices;
+  p.topk_length = topk_length;
+  p.attn_sink = attn_sink;
+  p.lse = lse;
+  p.out = static_cast<const __nv_bfloat16*>(out);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.dq = dq;
+  p.dkv = dkv;
+  p.dsink = attn_sink ? dsink : nullptr;
+  p.sm_scale = sm_scale;
+  p.s_q = s_q;
+  p.s_kv = s_kv;
+  p.h_q = h_q;
+  p.topk = topk;
+  p.n_groups = h_q / kGroupHeads;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  const int64_t n_items = s_q * p.n_groups;
+  return d_qk == 512 ? launch_bwd<512>(qm, dom, kvm, p, n_items, stream)
+                     : launch_bwd<576>(qm, dom, kvm, p, n_items, stream);
+}

@@ -1117,6 +1117,9 @@ smla_status check_common(const void* q, const void* kv, const int32_t* indices, 
 
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 
+// the backward kernel and its host side share the helpers above
+#include "sparse_mla_bwd.cuh"
+
 }  // namespace
 }  // namespace smla
 
@@ -1354,6 +1357,14 @@ const char* sparse_mla_status_string(smla_status s) {
 }
 
 int sparse_mla_abi_version(void) { return SMLA_ABI_VERSION; }
+
+smla_status sparse_mla_bwd(const void* q, const void* kv, const void* out, const void* dout,
+                           const int32_t* indices, const int32_t* topk_length, const float* attn_sink,
+                           const float* lse, float sm_scale, int d_v, float* dq, float* dkv, float* dsink,
+                           int64_t s_q, int64_t s_kv, int h_q, int d_qk, int topk, smla_stream_t stream) {
+  return smla::bwd_flat(q, kv, out, dout, indices, topk_length, attn_sink, lse, sm_scale, d_v, dq, dkv, dsink,
+                        s_q, s_kv, h_q, d_qk, topk, reinterpret_cast<cudaStream_t>(stream));
+}
 
 #ifdef SMLA_TRACE
 // Debug builds only: copies the pipeline trace of CTA 0 ([256 blocks][12 events] int64 clock

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.sparse_mla_abi_version() == 2
+    assert lib.sparse_mla_abi_version() == 3
     for code in range(8):
         s = smla.sparse_mla_status_string(code)
         assert s and s != "unknown status"
@@ -115,3 +115,20 @@ def test_splitkv_workspace_size_and_argument_checks(lib):
     assert call(nbytes=1000) == 7                   # too small
     assert call(ws=FAKE + 16) == 3                  # not 256-byte aligned
     assert call(s_q=0, q=None, kv=None, idx=None, out=None) == 0
+
+
+def call_bwd(lib, q=FAKE, kv=FAKE, out=FAKE, dout=FAKE, idx=FAKE, tl=None, sink=None, lse=FAKE, scale=0.04,
+             d_v=512, dq=FAKE, dkv=FAKE, dsink=None, s_q=4, s_kv=16, h_q=64, d_qk=576, topk=8):
+    return lib.sparse_mla_bwd(q, kv, out, dout, idx, tl, sink, lse, ctypes.c_float(scale), d_v, dq, dkv, dsink,
+                              s_q, s_kv, h_q, d_qk, topk, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h_q=48), 2), (dict(d_qk=256), 2), (dict(d_v=256), 2), (dict(topk=0), 2), (dict(s_kv=-1), 2),
+    (dict(scale=-1.0), 2), (dict(q=None), 1), (dict(idx=None), 1), (dict(lse=None), 1), (dict(dq=None), 1),
+    (dict(out=None), 1), (dict(dout=None), 1), (dict(dkv=None), 1), (dict(out=FAKE + 8), 3),
+    (dict(dout=FAKE + 4), 3), (dict(q=FAKE + 2), 3), (dict(dkv=FAKE + 2), 3), (dict(dsink=FAKE + 1), 3),
+    (dict(sink=FAKE + 2), 3), (dict(tl=FAKE + 2), 3),
+])
+def test_bwd_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert call_bwd(lib, **kw) == code

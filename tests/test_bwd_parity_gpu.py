@@ -1,0 +1,95 @@
+"""GPU parity of the sparse MLA backward against the fp64 oracle (oracle/sparse_mla_bwd_oracle.c).
+
+The CUDA forward produces out / lse, the CUDA backward the gradients; the oracle recomputes the
+exact gradients of sum(dout * O) from q, kv and dout alone.  Acceptance:
+  * bit-exact: dq is exactly 0 on rows without a counted slot, dkv exactly 0 on kv rows no
+    counted slot selects;
+  * elsewhere, per tensor, relative L2 error <= 1e-2 and max-abs error <= 3e-2 * max|ref|.
+The tolerance follows from the arithmetic: P and sm_scale * dS enter the tensor-core products
+as bf16 (unit roundoff 2^-9), D = <dout, out> uses the forward's bf16 out, and everything is
+accumulated in fp32; independent rounding of that size leaves a relative L2 error of a few
+2^-9 (~0.5 %).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_mla_attention_fwd_gb300 as smla
+import workloads as W
+from gpu_helpers import dev_tensor
+
+REL_L2 = 1e-2
+MAX_REL = 3e-2
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, dout):
+    q, kv, idx = dev_tensor(w["q"]), dev_tensor(w["kv"]), dev_tensor(w["indices"])
+    tl, sink = dev_tensor(w["topk_length"]), dev_tensor(w["attn_sink"])
+    out, lse, _ = smla.sparse_mla_fwd(q, kv, idx, tl, sink, sm_scale=w["sm_scale"])
+    dq, dkv, ds = smla.sparse_mla_bwd(q, kv, out, dev_tensor(dout), idx, lse, tl, sink, sm_scale=w["sm_scale"])
+    torch.cuda.synchronize()
+    assert smla.sparse_mla_device_status(reset=True) == 0
+    return dq.cpu().numpy(), dkv.cpu().numpy(), None if ds is None else ds.cpu().numpy()
+
+
+def _close(got, ref, name):
+    err = got.astype(np.float64) - ref
+    scale = float(np.abs(ref).max())
+    rel = float(np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30))
+    assert rel <= REL_L2, f"{name}: relative L2 error {rel:.3e}"
+    assert float(np.abs(err).max()) <= MAX_REL * max(scale, 1e-30), f"{name}: max-abs error {np.abs(err).max():.3e}"
+
+
+def _counted(w):
+    idx = w["indices"].reshape(w["indices"].shape[0], -1)
+    s_kv = w["kv"].shape[0]
+    ok = (idx >= 0) & (idx < s_kv)
+    if w["topk_length"] is not None:
+        ok &= np.arange(idx.shape[1])[None, :] < np.clip(w["topk_length"], 0, idx.shape[1])[:, None]
+    return idx, ok
+
+
+CASES = [
+    # seed, s_q, s_kv, h_q, d_qk, topk, with_len, with_sink, dup
+    (1, 64, 900, 64, 576, 200, True, True, True),
+    (2, 40, 700, 128, 512, 130, False, False, False),
+    (3, 24, 5000, 64, 576, 1024, False, True, False),
+    (4, 32, 333, 64, 512, 64, True, True, True),
+    (5, 16, 2000, 128, 576, 96, True, False, False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"s{c[0]}_h{c[3]}_d{c[4]}_k{c[5]}" for c in CASES])
+def test_bwd_matches_oracle(case):
+    seed, s_q, s_kv, h_q, d_qk, topk, with_len, with_sink, dup = case
+    w = W.random_case(seed, s_q, s_kv, h_q, d_qk, topk, with_len=with_len, with_sink=with_sink,
+                      poison_suffix=with_len, dup=dup)
+    dout = W.dout_for(w, salt=seed)
+    dq, dkv, ds = _run(w, dout)
+    rq, rkv, rs = oracle.sparse_mla_bwd(w["q"], w["kv"], dout, w["indices"], w["topk_length"], w["attn_sink"],
+                                        w["sm_scale"])
+    idx, ok = _counted(w)
+    empty = ~ok.any(axis=1)
+    assert empty.any() or s_q < 8
+    assert np.all(dq[empty] == 0.0), "dq of rows without a counted slot must be exactly 0"
+    untouched = np.ones(s_kv, bool)
+    untouched[np.unique(idx[ok])] = False
+    assert np.all(dkv[untouched] == 0.0), "dkv rows no slot selects must be exactly 0"
+    _close(dq, rq, "dq")
+    _close(dkv, rkv, "dkv")
+    if with_sink:
+        _close(ds, rs, "dsink")
+    else:
+        assert ds is None
+
+
+def test_bwd_dq_is_deterministic_and_dkv_stable():
+    w = W.random_case(6, 32, 800, 64, 576, 192, with_sink=True)
+    dout = W.dout_for(w, salt=6)
+    a = _run(w, dout)
+    b = _run(w, dout)
+    np.testing.assert_array_equal(a[0], b[0])          # dq: no atomics
+    np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-4 * float(np.abs(a[1]).max()))

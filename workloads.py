@@ -271,3 +271,22 @@ def valid_slot_count(indices, s_kv, topk_length=None):
         L = np.clip(np.asarray(topk_length), 0, idx.shape[1])
         ok &= np.arange(idx.shape[1])[None, :] < L[:, None]
     return ok.sum(axis=1)
+
+
+def dout_for(w, salt: int = 17):
+    """Seeded N(0,1) bf16 gradient of the loss w.r.t. O ([s_q, h_q, d_v] bit patterns) for the
+    backward: the upstream gradient a training step would feed in."""
+    s_q, h_q = w["q"].shape[0], w["q"].shape[1]
+    rng = np.random.Generator(np.random.PCG64(SEED_BASE + 104729 * salt + s_q))
+    return normal_bf16(rng, (s_q, h_q, w["d_v"]))
+
+
+def bwd_prefill(s_q=4096, s_kv=32768, h_q=64, d_qk=576, topk=2048, config_no=8):
+    """Backward benchmark shape of FlashMLA PR #198 ("Numerics": T = 4096, topk = 2048; "Notes":
+    h_q = 64, d_qk = 576): every row holds topk distinct uniform indices in [0, s_kv), no
+    invalid entry, no topk_length, no sink."""
+    rng = rng_for(config_no)
+    q = normal_bf16(rng, (s_q, h_q, d_qk))
+    kv = normal_bf16(rng, (s_kv, 1, d_qk))
+    idx = distinct_rows(rng, s_q, topk, s_kv)
+    return _base("bwd_prefill", q, kv, idx.reshape(s_q, 1, topk), None, None, s_kv=s_kv)
