@@ -6,8 +6,12 @@ run WITHOUT topk_length -- the kernel derives each row's length itself.  One ste
 of the whole forward on that batch.  The metric is valid-token TFLOP/s,
 2*h_q*valid*(d_qk+d_v) summed over rows, divided by the device time of the call.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config ramp|full|scattered|decode|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config ramp|full|scattered|decode|tiny|bwd]
                   [--impl ours|reference]
+
+--config bwd times the backward instead (sparse_mla_bwd on s_q=4096, s_kv=32768, h_q=64,
+d_qk=576, topk=2048, all valid): one step = one backward call given the forward's out / lse,
+metric = 2*h_q*valid*(3*d_qk + 2*d_v) FLOPs (S and dP recomputed, dQ, dK, dV) per second.
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch of the same shape (weak
 scaling, no collective on the data path); the time is the max over ranks.
@@ -33,6 +37,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "sparse-MLA fwd ms/call & valid-token TFLOP/s; % of GB300 bf16 tensor peak"
+METRIC_BWD = "sparse-MLA bwd ms/call & valid-token TFLOP/s; % of GB300 bf16 tensor peak"
 UNIT = "TFLOP/s"
 # FlashMLA PR #196 "Numbers" (B200, not GB300): ramp-padded, no topk_length, 1.144 ms for
 # 1.0337 TFLOP of valid-token work -> 903.6 TFLOP/s.  Context only.
@@ -47,7 +52,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["ramp", "full", "scattered", "decode", "decode_b2", "decode_b8", "tiny"],
+    ap.add_argument("--config", choices=["ramp", "full", "scattered", "decode", "decode_b2", "decode_b8", "tiny",
+                                         "bwd"],
                     default="ramp")
     ap.add_argument("--n-split", default="auto",
                     help="split-KV ranges per row: 'auto' (split only when items < SMs) or an integer")
@@ -72,6 +78,8 @@ def make_workload(name, with_len):
         return W.decode_fixed(n_req=2)
     if name == "decode_b8":
         return W.decode_fixed(n_req=8)
+    if name == "bwd":
+        return W.bwd_prefill()
     return W.tiny(with_len=with_len, with_sink=True)
 
 
@@ -92,11 +100,14 @@ def describe(w, name):
         "decode_b8": f"small-batch paged decode B=8 x S_q=2 s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} d_v=512 "
                      f"topk={topk} all valid, 64-token pages",
         "tiny": f"tiny s_q={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} topk={topk}",
+        "bwd": f"sparse backward s_q={s_q} s_kv={w['s_kv']} h_q={h_q} d_qk={d_qk} d_v=512 topk={topk} all valid",
     }[name]
     return text
 
 
-def valid_flops(w, rows=None):
+def valid_flops(w, rows=None, backward=False):
+    """Valid-token FLOPs: forward 2*h_q*(d_qk + d_v) per counted slot; backward
+    2*h_q*(3*d_qk + 2*d_v) (S and dP recomputed, then dQ, dK and dV)."""
     idx = w["indices"].reshape(w["q"].shape[0], -1)
     tl = w["topk_length"]
     if rows is not None:
@@ -104,7 +115,8 @@ def valid_flops(w, rows=None):
         tl = None if tl is None else np.asarray(tl)[rows]
     counts = W.valid_slot_count(idx, w["s_kv"], tl)
     h_q, d_qk = w["q"].shape[1], w["q"].shape[2]
-    return float(2.0 * h_q * counts.sum() * (d_qk + w["d_v"]))
+    per = (3 * d_qk + 2 * w["d_v"]) if backward else (d_qk + w["d_v"])
+    return float(2.0 * h_q * counts.sum() * per)
 
 
 def load_peaks():
@@ -230,6 +242,9 @@ def run_reference(args, world, rank):
     import oracle
 
     w = make_workload(args.config, args.with_len)
+    bwd = args.config == "bwd"
+    if bwd:
+        w["backward"], w["dout"] = True, W.dout_for(w)
     s_q = w["q"].shape[0]
     cores = len(os.sched_getaffinity(0))
     per_step = max(1, cores)
@@ -243,10 +258,10 @@ def run_reference(args, world, rank):
         t0 = time.perf_counter()
         _oracle_call(oracle, w, rows)
         t_total += time.perf_counter() - t0
-        flops += valid_flops(w, rows)
+        flops += valid_flops(w, rows, backward=bwd)
     value = flops / t_total / 1e12
     sample = f"{per_step} random rows per step of the {args.config} batch ({args.steps} steps)"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
@@ -257,6 +272,10 @@ def run_reference(args, world, rank):
 
 
 def _oracle_call(oracle, w, rows):
+    if w.get("backward"):
+        q = w["q"][rows]
+        idx = w["indices"].reshape(w["q"].shape[0], -1)[rows]
+        return oracle.sparse_mla_bwd(q, w["kv"], w["dout"][rows], idx, None, None, w["sm_scale"])
     if w.get("paged"):
         return oracle.sparse_mla_fwd_paged(w["q"], w["kv"], w["block_table"], w["indices"], w["page_block"],
                                            w.get("seqlens_k"), w["s_kv_per_req"], w["s_q_per_req"],
@@ -281,7 +300,7 @@ def cpu_baseline(w, name, budget_s=12.0):
         t0 = time.perf_counter()
         _oracle_call(oracle, w, rows)
         t_total += time.perf_counter() - t0
-        flops += valid_flops(w, rows)
+        flops += valid_flops(w, rows, backward=bool(w.get("backward")))
         done += len(rows)
     return {"value": flops / t_total / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{done} random rows of the {name} batch ({t_total:.1f} s of fp64 CPU work)"}
@@ -310,6 +329,8 @@ def main():
             dist.barrier()
 
     w = make_workload(args.config, args.with_len)
+    if args.config == "bwd":
+        return main_bwd(args, w, world, rank, local, dev, barrier)
     s_q, h_q, d_qk = w["q"].shape
     flops = valid_flops(w)
 
@@ -464,6 +485,112 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def main_bwd(args, w, world, rank, local, dev, barrier):
+    """The backward: each step is one sparse_mla_bwd call on the batch, given the forward's out
+    and lse (computed once, outside the timed region)."""
+    import torch
+
+    import sparse_mla_attention_fwd_gb300 as smla
+
+    w["backward"], w["dout"] = True, W.dout_for(w)
+    s_q, h_q, d_qk = w["q"].shape
+    s_kv = w["kv"].shape[0]
+    flops = valid_flops(w, backward=True)
+    stream = torch.cuda.current_stream(dev)
+
+    def host_tensor(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.pin_memory()
+
+    host = {k: host_tensor(w[k]) for k in ("q", "kv", "indices", "dout")}
+    d = {k: v.to(dev) for k, v in host.items()}
+    out, lse, _ = smla.sparse_mla_fwd(d["q"], d["kv"], d["indices"], sm_scale=w["sm_scale"], stream=stream)
+    host["out"], host["lse"] = out.cpu().pin_memory(), lse.cpu().pin_memory()
+    d["out"], d["lse"] = out, lse
+    dq = torch.empty((s_q, h_q, d_qk), dtype=torch.float32, device=dev)
+    dkv = torch.empty((s_kv, d_qk), dtype=torch.float32, device=dev)
+
+    def call():
+        smla.sparse_mla_bwd(d["q"], d["kv"], d["out"], d["dout"], d["indices"], d["lse"], sm_scale=w["sm_scale"],
+                            dq=dq, dkv=dkv, stream=stream)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    steps = max(3, min(args.steps, 30))          # a call is tens of ms: bound the timed work
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.3 if not args.no_clocks else 0.0)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(float(np.sum(step_ms)), dev)
+    ms_per_step = total_ms / steps
+    job_flops = sum_over_ranks(flops, dev)
+    value = job_tflops(job_flops * steps, total_ms)
+
+    e2e = None
+    if not args.skip_e2e:
+        dq_h = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+        dkv_h = torch.empty(dkv.shape, dtype=dkv.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = dq.numel() * 4 + dkv.numel() * 4
+        e_ms = []
+        for i in range(4):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k, v in host.items():
+                d[k].copy_(v, non_blocking=True)
+            call()
+            dq_h.copy_(dq, non_blocking=True)
+            dkv_h.copy_(dkv, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 1:
+                e_ms.append(a.elapsed_time(b))
+        e2e_ms = max_over_ranks(float(np.mean(e_ms)), dev)
+        e2e = {"value": job_tflops(job_flops, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+    status = smla.sparse_mla_device_status()
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe(w, "bwd"), "topk_length": "omitted",
+                   "l2": "flushed (256 MB write) between timed iterations",
+                   "pct_of_bf16_peak": 100.0 * achieved / peak},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic("bwd"),
+                     "peak_source": f"bf16_tflops burst ({src})", "kernel": "sparse_mla_bwd_kernel"},
+        "clocks": clocks, "gpu_launches": steps, "device_status": status,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.skip_cpu and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, "bwd")
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

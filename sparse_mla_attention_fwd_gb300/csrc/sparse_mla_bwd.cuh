@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       wait_or_flag(smem_u32(&bar_qdo_full), 0, abort, lim);
       for (int b = 0; b < nb && !*abort; ++b) {
         wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);
+        SMLA_TRACE_EVENT(b, kTrGatherIssue);
         // S and dP reuse the columns of dKV^T buffers 1 and 2: every drain of them is done
         if (xu[1] > 0) wait_or_flag(smem_u32(&bar_x_free[1]), (xu[1] - 1) & 1, abort, lim);
         if (xu[2] > 0) wait_or_flag(smem_u32(&bar_x_free[2]), (xu[2] - 1) & 1, abort, lim);
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ss(tmem + kBwdTmemDP, do_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&bar_s_full));
+        SMLA_TRACE_EVENT(b, kTrQkIssue);
         wait_or_flag(smem_u32(&bar_p_full), b & 1, abort, lim);
         tc_fence_after();
         // dQ^T += K^T dS'^T over this block's 64 keys
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     (b > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(smem_u32(&bar_kv_empty));          // S, dP and dQ^T have read the stage
+        SMLA_TRACE_EVENT(b, kTrPvIssue);
         // dKV^T chunk c = Q^T dS' (+ dO^T P on the value rows), one buffer of three each
 #pragma unroll
         for (int c = 0; c < kDkvChunks; ++c) {
@@ -204,6 +207,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ++xu[i];
         }
         umma_commit(smem_u32(&bar_tiles_free));        // P and dS' tiles may be rewritten
+        SMLA_TRACE_EVENT(b, kTrEpilogue);
       }
       umma_commit(smem_u32(&bar_dq_full));
       umma_commit(smem_u32(&bar_final));
@@ -261,6 +265,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int sb = b & 1;
       wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);   // also publishes s_rows[sb]
       wait_or_flag(smem_u32(&bar_s_full), b & 1, abort, lim);
+      SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrSReady);
       tc_fence_after();
       float sv[32], dv[32];
 #pragma unroll
@@ -298,11 +303,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_p_full));
+      SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrPReady);
       // drain this block's dKV^T chunks into fp32 reductions on the selected kv rows
 #pragma unroll
       for (int c = 0; c < kDkvChunks; ++c) {
         const int i = c % 3;
         wait_or_flag(smem_u32(&bar_x_full[i]), xu[i] & 1, abort, lim);
+        SMLA_TRACE_EVENT_IF(c == 0 && q == 0 && lane == 0, b, kTrSLoaded);
         ++xu[i];
         tc_fence_after();
         const bool rope = kRope && c == 4;
@@ -330,7 +337,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-    // ---- dq of this item: dQ^T chunk c holds rows d, columns = heads
+    // ---- dq of this item: dQ^T chunk c holds rows d, columns = heads (the last block's drains
+    // end here)
+    SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, nb, kTrSent);
     float* dq = p.dq + qrow * D_QK;
     if (nb > 0) {
       wait_or_flag(smem_u32(&bar_dq_full), 0, abort, lim);
@@ -371,6 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int grp = it & 15, chunk = it >> 4;
     for (int b = 0; b < nb && !*abort; ++b) {
       if (b >= 1) wait_or_flag(smem_u32(&bar_kv_empty), (b - 1) & 1, abort, lim);
+      SMLA_TRACE_EVENT_IF(leader, b, kTrRing);
       if (gw == 0) {
         s_rows[b & 1][lane] = bwd_row(p, idx_row, 64 * b + lane, L);
         s_rows[b & 1][lane + 32] = bwd_row(p, idx_row, 64 * b + lane + 32, L);
