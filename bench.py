@@ -131,7 +131,8 @@ def load_peaks():
 def kernel_source_hash():
     h = hashlib.sha256()
     for rel in ("sparse_mla_attention_fwd_gb300/csrc/sparse_mla_fwd.cu",
-                "sparse_mla_attention_fwd_gb300/csrc/smla_ptx.cuh"):
+                "sparse_mla_attention_fwd_gb300/csrc/smla_ptx.cuh",
+                "sparse_mla_attention_fwd_gb300/csrc/sparse_mla_bwd.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -140,7 +141,8 @@ def kernel_source_hash():
 def profiled_traffic(config_name):
     """DRAM bytes per launch from the committed ncu summary for this workload, if it was taken
     on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"sparse_mla_fwd_{config_name}.md")
+    name = {"bwd": "sparse_mla_bwd_prefill.md"}.get(config_name, f"sparse_mla_fwd_{config_name}.md")
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
