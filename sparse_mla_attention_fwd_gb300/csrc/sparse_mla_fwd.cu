@@ -15,7 +15,7 @@
 // costs nothing (the fix of FlashMLA PR #196, "Fix") and neither do invalid entries inside the
 // row.
 //
-// Warp roles (384 threads, 12 warps = 3 per SM sub-partition, warp w on sub-partition w % 4):
+// Warp roles (512 threads, 16 warps = 4 per SM sub-partition, warp w on sub-partition w % 4):
 //   warps 0,1,3,8,9     gather    : TMA gather4 of the selected KV rows (whole rows: measured
 //                                   ~45% faster per byte than half rows) into a 2-stage ring,
 //                                   each stage handed over in four column groups.  A slot
@@ -31,17 +31,17 @@
 //                                   coordinates + validity mask + first/last flags) in a shared
 //                                   16-deep ring.  It runs ahead, so index loads never sit on
 //                                   the critical path.
-// With d_qk = 512 a fourth warpgroup (warps 12-15, 512 threads) copies value columns 0..255 of
-// each gathered block into TMEM as V^T and also issues gathers; setmaxnreg gives the softmax
-// warpgroup 200 registers and the others 104.
+//   warps 12-15         V^T       : copy value columns 0..255 of each gathered block into TMEM
+//                                   as V^T (ldmatrix.trans -> tcgen05.st) and issue gathers.
+// setmaxnreg gives the softmax warpgroup 200 registers and the other three 104.
 // Tensor-core work per 64-key block:
 //   S[64 heads x 64 keys]  = Q_g . K_blk^T        (M=64, N=64, K=d_qk; both K-major SW128)
-//   O^T[512 x 64 heads]   += V_blk^T . P^T        (4 x M=128, N=64, K=64; V^T read MN-major
-//                                                  straight out of the gathered block, or for
-//                                                  value columns 0..255 with d_qk = 512, out
-//                                                  of TMEM)
-// TMEM: O^T in columns [0,256), S double buffer in [256,384), with d_qk = 512 a V^T double
-// buffer (value columns 0..255) in [384,512).
+//   O^T[512 x 64 heads]   += V_blk^T . P^T        (4 x M=128, N=64, K=64; V^T of value columns
+//                                                  256..511 read MN-major straight out of the
+//                                                  gathered block, of columns 0..255 out of
+//                                                  TMEM)
+// TMEM: O^T in columns [0,256), S double buffer in [256,384), V^T double buffer (value columns
+// 0..255) in [384,512).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -62,16 +62,13 @@ namespace {
 constexpr int kBlockN = 64;            // keys per k-block
 constexpr int kGroupHeads = 64;        // heads per work item
 constexpr int kDv = 512;               // value width (first d_v columns of each kv row)
-// 12 warps = 3 per SM sub-partition (warp w runs on sub-partition w % 4), so each thread may
-// hold up to 168 registers.  S = QK^T and O^T += V^T P^T are issued by two different threads:
-// the tensor unit interleaves two independent issue streams without the dead time a single
-// issuer leaves between chains (it is blocked inside each chain's issue until the chain has
-// nearly drained, then has to find the next ready chain).
-constexpr int kThreads = 384;
-// d_qk = 512 adds a fourth warpgroup (warps 12-15, TMEM lane quadrants 0-3) that copies V^T
-// into TMEM; registers are then rebalanced towards the softmax warpgroup.
-template <int D_QK>
-constexpr int threads_for() { return D_QK == 512 ? 512 : kThreads; }
+// 16 warps = 4 per SM sub-partition (warp w runs on sub-partition w % 4).  S = QK^T and
+// O^T += V^T P^T are issued by two different threads: the tensor unit interleaves two
+// independent issue streams without the dead time a single issuer leaves between chains (it is
+// blocked inside each chain's issue until the chain has nearly drained, then has to find the
+// next ready chain).  The fourth warpgroup (warps 12-15, TMEM lane quadrants 0-3) copies V^T
+// into TMEM and gathers; registers are rebalanced towards the softmax warpgroup.
+constexpr int kThreads = 512;
 constexpr int kVtWarp0 = 12;
 constexpr int kSoftmaxRegs = 200;      // setmaxnreg split of the 512-thread kernel: 128 x 200
 constexpr int kOtherRegs = 104;        // + 384 x 104 = 65536 = 512 threads x 128 at launch
@@ -81,12 +78,11 @@ constexpr int kQkWarp = 2;             // QK issuer; also allocates TMEM and loa
 constexpr int kPvWarp = 11;            // PV issuer
 constexpr int kSchedWarp = 10;
 constexpr int kRing = 16;              // scheduler ring depth (blocks)
-constexpr int kRingConsumers = kGatherWarps + 4 + 2;   // arrivals that free a ring slot
-constexpr int kRingConsumersVT = kRingConsumers + 4;   // ... with the V^T warpgroup
+constexpr int kRingConsumers = kGatherWarps + 4 + 2 + 4;   // gather, softmax, 2 issuers, V^T
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O^T: 4 chunks x 64 columns
 constexpr uint32_t kTmemS = 256;       // S buffers: 256 + 64*b
-constexpr uint32_t kTmemVT = 384;      // d_qk = 512: V^T of value chunks 0-1, 2 buffers x 2 x 32
+constexpr uint32_t kTmemVT = 384;      // V^T of value chunks 0-1: 2 buffers x 2 chunks x 32 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the running max grows by > 2^8
@@ -212,7 +208,7 @@ __device__ __forceinline__ int kv_row_of(const FwdParams& p, int64_t t, int v) {
 // SPLIT: work units are (item, slot range); the epilogue writes the unit's partial result to
 // the split-KV workspace instead of O / lse / max_logits (a second kernel merges the ranges).
 template <int D_QK, bool DYNAMIC, bool PAGED, bool SPLIT>
-__global__ void __launch_bounds__(threads_for<D_QK>(), 1)
+__global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_fwd_kernel(const __grid_constant__ CUtensorMap q_map,
                           const __grid_constant__ CUtensorMap kv_map, const FwdParams p) {
   constexpr int kChunks = D_QK / 64;                 // 128-byte column chunks of a row
@@ -227,14 +223,13 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
   // columns, so group g of a stage is refilled as soon as PV M-chunk g of the block before has
   // completed, and S = QK^T of the new block starts on group 0 while later groups are in flight.
   constexpr int kGroups = 4;
-  // With d_qk = 512 (no rope chunk) PV reads value chunks 0-1 (columns 0..255) as V^T out of
-  // TMEM, double-buffered in the 128 columns that O^T and S leave free; chunks 2-3 it reads
-  // from the stage as usual.  The V^T warps copy column groups 0-1 of a stage into TMEM
-  // (ldmatrix.trans -> tcgen05.st) as soon as they land, so those groups are released once
-  // S = QK^T and the copy have read them, well before PV; the gather of groups 0-1 of block
-  // b+2 then overlaps PV of block b, and QK(b+2) streams through them while groups 2-3 are in
-  // flight.  (With a rope chunk the stage also holds P^T, so it stays until PV ends.)
-  constexpr bool kVT = (kChunks == 8);
+  // PV reads value chunks 0-1 (columns 0..255) as V^T out of TMEM, double-buffered in the 128
+  // columns that O^T and S leave free; chunks 2-3 it reads from the stage as usual.  The V^T
+  // warps copy column groups 0-1 of a stage into TMEM (ldmatrix.trans -> tcgen05.st) as soon
+  // as they land, so those groups are released once S = QK^T and the copy have read them, well
+  // before PV; the gather of groups 0-1 of block b+2 then overlaps PV of block b, and QK(b+2)
+  // streams through them while groups 2-3 are in flight.  With a rope chunk, P^T lives in it,
+  // so group 3 goes back only after PV's last M-chunk.
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -274,16 +269,16 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
     abort_flag = 0;
     for (int r = 0; r < kRing; ++r) {
       mbar_init(smem_u32(&bar_ring_full[r]), 1);
-      mbar_init(smem_u32(&bar_ring_empty[r]), kVT ? kRingConsumersVT : kRingConsumers);
+      mbar_init(smem_u32(&bar_ring_empty[r]), kRingConsumers);
     }
     mbar_init(smem_u32(&bar_q_full), 1);
     mbar_init(smem_u32(&bar_q_empty), 1);
     for (int s = 0; s < 2; ++s) {
       for (int g = 0; g < kGroups; ++g) {
         mbar_init(smem_u32(&bar_kv_full[s][g]), 1);
-        // released by PV (one commit), or for groups 0-1 with V^T in TMEM by S = QK^T (one
-        // commit) and the four V^T warps
-        mbar_init(smem_u32(&bar_kv_empty[s][g]), (kVT && g < 2) ? 5 : 1);
+        // groups 0-1 are released by S = QK^T (one commit) and the four V^T warps, groups 2-3
+        // by PV (one commit)
+        mbar_init(smem_u32(&bar_kv_empty[s][g]), g < 2 ? 5 : 1);
       }
       mbar_init(smem_u32(&bar_s_full[s]), 1);
       mbar_init(smem_u32(&bar_p_full[s]), 128);
@@ -310,7 +305,7 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
   // Roles.  The softmax warpgroup comes first so that, in the 512-thread kernel, its code is
   // dominated by the register increase and every other role by the decrease.
   if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
-    if constexpr (kVT) reg_alloc<kSoftmaxRegs>();
+    reg_alloc<kSoftmaxRegs>();
     // ======================================================== softmax / correction / epilogue
     const int q = warp - kSoftmaxWarp0;          // TMEM lane quadrant 0..3
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -394,11 +389,12 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
         }
         // P as bf16 into the P^T operand tile ([64 heads][64 keys], 128-byte swizzle).  Its
         // previous user (block b-2) finished its PV before the stage was refilled for block b,
-        // which S(b) being ready already implies -- except with V^T in TMEM, where PV's last
-        // M-chunks read TMEM and not the stage, so PV(b-2) is waited for here.  Masked slots hold
+        // which S(b) being ready already implies when P^T lives in the stage's rope chunk.  The
+        // separate P^T buffer (no rope chunk) has no such link -- PV's last M-chunks read TMEM,
+        // not the stage -- so PV(b-2) is waited for here.  Masked slots hold
         // -inf and give exp2(-inf) = 0; a row whose offset is still -inf has no valid slot yet,
         // and any finite offset then yields 0 as well.
-        if (kVT && b >= 2) wait_or_flag(smem_u32(&bar_o_done[sb]), ((b - 2) >> 1) & 1, abort, lim);
+        if (!kPInStage && b >= 2) wait_or_flag(smem_u32(&bar_o_done[sb]), ((b - 2) >> 1) & 1, abort, lim);
         const float neg_m0 = m_used[0] == -INFINITY ? 0.f : -m_used[0];
         const float neg_m1 = m_used[1] == -INFINITY ? 0.f : -m_used[1];
         uint8_t* ptile = p_addr(static_cast<int>(b));
@@ -530,7 +526,7 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
       }
     }
   } else {
-    if constexpr (kVT) reg_dealloc<kOtherRegs>();
+    reg_dealloc<kOtherRegs>();
     if (warp == kSchedWarp) {
       // ======================================================== scheduler
       // Per row, a parallel scan first finds the last counted slot (j < L_t, 0 <= idx < s_kv) and
@@ -677,12 +673,12 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
         publish(lastb, m0, m1, (lastb == b0 ? kFirstBlock : 0u) | kLastBlock, item);
         b = lastb + 1;
       }
-    } else if (warp < 2 || warp == 3 || warp == 8 || warp == 9 || (kVT && warp >= kVtWarp0)) {
+    } else if (warp < 2 || warp == 3 || warp == 8 || warp == 9 || warp >= kVtWarp0) {
       // ======================================================== gather (+ V^T copies)
       // TMA issue throughput grows with the number of issuing warps, so the 16 x (chunks of a
       // group) gather4 items of each column group are dealt round-robin over the gather warps:
-      // warps 0, 1, 3, 8, 9, and with d_qk = 512 also the four V^T warps 12-15.
-      constexpr int kGW = kVT ? kGatherWarps + 4 : kGatherWarps;
+      // warps 0, 1, 3, 8, 9 and the four V^T warps 12-15.
+      constexpr int kGW = kGatherWarps + 4;
       // gather warp index 0..kGW-1: warps 0, 1, 3, 8, 9 -> 0..4, warps 12-15 -> 5..8
       const int gw = warp < 2 ? warp
                    : warp == 3 ? 2
@@ -700,7 +696,7 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
       // 2c, 2c+1 of TMEM column c = 8x + 4(i>>1) + (t&3): natural key order.  The copy of block
       // j comes in the middle of this warp's gathers for block j+1 and before those for block
       // j+2, which wait for it (through kv_empty).
-      const bool vt_warp = kVT && warp >= kVtWarp0;
+      const bool vt_warp = warp >= kVtWarp0;
       auto copy_vt = [&](int64_t j) {
         const int q = warp - kVtWarp0;
         const int mat = lane >> 3, rr = lane & 7;
@@ -819,7 +815,7 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
                 umma_ss(tmem + kTmemS + 64 * s, qd0 + off16, kd0 + off16, idesc_qk, ks > 0 ? 1u : 0u);
               }
               // with V^T in TMEM, PV does not read groups 0-1 of the stage: S = QK^T releases them
-              if (kVT && g < 2) umma_commit(smem_u32(&bar_kv_empty[s][g]));
+              if (g < 2) umma_commit(smem_u32(&bar_kv_empty[s][g]));
             }
             umma_commit(smem_u32(&bar_s_full[s]));
             SMLA_TRACE_EVENT(b, kTrSLoaded);
@@ -862,42 +858,30 @@ __global__ void __launch_bounds__(threads_for<D_QK>(), 1)
             SMLA_TRACE_EVENT(b, kTrPvIssue);
             // descriptor start addresses advance in 16-byte units (low 14 bits)
             const uint64_t b0 = make_sdesc_sw128(smem_u32(p_addr(static_cast<int>(b))), 16, 1024);
-            if constexpr (kVT) {
-              // M-chunks 2-3 from the stage first (that frees its column groups 2-3), then 0-1
-              // from V^T buffer b&1 in TMEM
-              const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
+            // M-chunks 2-3 from the stage first (that frees its column groups 2-3), then 0-1 from
+            // V^T buffer b&1 in TMEM
+            const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
 #pragma unroll
-              for (int m = 2; m < 4; ++m) {
+            for (int m = 2; m < 4; ++m) {
 #pragma unroll
-                for (int ks = 0; ks < kBlockN / 16; ++ks)
-                  umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
-                          b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
-                umma_commit(smem_u32(&bar_kv_empty[sb][m]));
-              }
-#pragma unroll
-              for (int m = 0; m < 2; ++m) {
-                wait_or_flag(smem_u32(&bar_vt_full[sb][m]), (b >> 1) & 1, abort, lim);
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < kBlockN / 16; ++ks)
-                  umma_ts(tmem + kTmemO + 64 * m, tmem + kTmemVT + 64 * sb + 32 * m + 8 * ks,
-                          b0 + ((ks * 32) >> 4), idesc_pv_ts, (!first || ks > 0) ? 1u : 0u);
-                umma_commit(smem_u32(&bar_vt_free[sb][m]));   // V^T buffer sb, chunk m reusable
-              }
-            } else {
-              const uint64_t a0 = make_sdesc_sw128(kv_base + sb * kTileBytes, 8192, 1024);
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-#pragma unroll
-                for (int ks = 0; ks < kBlockN / 16; ++ks) {
-                  umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
-                          b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
-                }
-                // column group m of this stage has been read by every MMA that needs it (the
-                // last group's commit also covers P^T in the rope chunk)
-                umma_commit(smem_u32(&bar_kv_empty[sb][m]));
-              }
+              for (int ks = 0; ks < kBlockN / 16; ++ks)
+                umma_ss(tmem + kTmemO + 64 * m, a0 + ((2 * m * 8192 + ks * 2048) >> 4),
+                        b0 + ((ks * 32) >> 4), idesc_pv, (!first || ks > 0) ? 1u : 0u);
+              // with P^T in the rope chunk (group 3), group 3 goes back only after the last
+              // PV M-chunk has read P^T
+              if (!kPInStage || m == 2) umma_commit(smem_u32(&bar_kv_empty[sb][m]));
             }
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              wait_or_flag(smem_u32(&bar_vt_full[sb][m]), (b >> 1) & 1, abort, lim);
+              tc_fence_after();
+#pragma unroll
+              for (int ks = 0; ks < kBlockN / 16; ++ks)
+                umma_ts(tmem + kTmemO + 64 * m, tmem + kTmemVT + 64 * sb + 32 * m + 8 * ks,
+                        b0 + ((ks * 32) >> 4), idesc_pv_ts, (!first || ks > 0) ? 1u : 0u);
+              umma_commit(smem_u32(&bar_vt_free[sb][m]));   // V^T buffer sb, chunk m reusable
+            }
+            if constexpr (kPInStage) umma_commit(smem_u32(&bar_kv_empty[sb][3]));
             umma_commit(smem_u32(&bar_o_done[sb]));
             SMLA_TRACE_EVENT(b, kTrSent);
           }
@@ -1065,7 +1049,7 @@ smla_status launch_one(const CUtensorMap& qm, const CUtensorMap& kvm, const FwdP
   // assigned round-robin
   const int64_t units = SPLIT ? p.n_items * p.n_split : p.n_items;
   const int64_t grid = units < sms ? units : sms;
-  kern<<<static_cast<unsigned>(grid), threads_for<D_QK>(), smem, stream>>>(qm, kvm, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(qm, kvm, p);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_LAUNCH;
   if constexpr (SPLIT) {
     splitkv_merge_kernel<<<dim3(static_cast<unsigned>(p.n_items), kGroupHeads / kMergeHeads), kMergeThreads, 0,
