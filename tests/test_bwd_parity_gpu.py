@@ -93,3 +93,25 @@ def test_bwd_dq_is_deterministic_and_dkv_stable():
     b = _run(w, dout)
     np.testing.assert_array_equal(a[0], b[0])          # dq: no atomics
     np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-4 * float(np.abs(a[1]).max()))
+
+
+def test_bwd_full_size_sampled_rows_and_column_sums():
+    """The backward on the bench shape (s_q 4096, s_kv 32768, h_q 64, d_qk 576, topk 2048) in the
+    launch configuration bench.py times.  dq of a row depends on that row alone, so sampled rows
+    are checked against the oracle one by one.  dkv is checked through a property that holds at
+    any size: without a sink, sum_s dS_s = D (1 - sum_s p_s) = 0 for every (row, head), so the
+    column sums of dkv are sum_{t,h} dO[t,h,d] on the value columns and 0 on the rope columns."""
+    w = W.bwd_prefill()
+    dout = W.dout_for(w)
+    dq, dkv, ds = _run(w, dout)
+    assert ds is None
+    rows = np.array([0, 1, 777, 2048, 3001, 4095])
+    idx = w["indices"].reshape(w["q"].shape[0], -1)
+    rq, _, _ = oracle.sparse_mla_bwd(w["q"][rows], w["kv"], dout[rows], idx[rows], None, None, w["sm_scale"])
+    _close(dq[rows], rq, "dq (sampled rows)")
+    d_v = w["d_v"]
+    ref = np.zeros(w["q"].shape[2])
+    ref[:d_v] = oracle.bf16_bits_to_f64(dout).sum(axis=(0, 1))
+    got = dkv.astype(np.float64).sum(axis=0)
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert rel <= REL_L2, f"dkv column sums: relative L2 error {rel:.3e}"
