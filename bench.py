@@ -128,11 +128,16 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel="fwd"):
+    """Hash of the sources that define a kernel: the forward's file and PTX wrappers, plus the
+    backward's own file for the backward (it is compiled in the forward's translation unit and
+    uses its helpers)."""
+    files = ["sparse_mla_attention_fwd_gb300/csrc/sparse_mla_fwd.cu",
+             "sparse_mla_attention_fwd_gb300/csrc/smla_ptx.cuh"]
+    if kernel == "bwd":
+        files.append("sparse_mla_attention_fwd_gb300/csrc/sparse_mla_bwd.cuh")
     h = hashlib.sha256()
-    for rel in ("sparse_mla_attention_fwd_gb300/csrc/sparse_mla_fwd.cu",
-                "sparse_mla_attention_fwd_gb300/csrc/smla_ptx.cuh",
-                "sparse_mla_attention_fwd_gb300/csrc/sparse_mla_bwd.cuh"):
+    for rel in files:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -148,7 +153,8 @@ def profiled_traffic(config_name):
     text = open(path).read()
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    kernel = "bwd" if config_name == "bwd" else "fwd"
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_bytes.group(1))
 

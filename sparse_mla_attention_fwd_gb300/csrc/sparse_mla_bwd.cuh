@@ -19,18 +19,32 @@
 //   dQ^T [d_qk x 64 heads] += K^T dS'^T           (M=128 (+64 for the rope), N=64, K=64 keys;
 //                                                  TMEM, accumulated over the row's blocks)
 //   dKV^T [d x 64 keys]     = Q^T dS' + dO^T P    (per 128-row chunk of d, K=64 heads; TMEM),
-//                             drained by the math warps into fp32 reductions on dkv
-// Warp roles (384 threads): warp 0 issues every MMA (one thread) and owns TMEM; warps 1-3 and
-// 8-11 gather the block's kv rows with TMA gather4 (warp 1 also loads the Q and dO tiles);
-// warps 4-7 (TMEM lane quadrants 0-3) compute P / dS', drain dKV^T and write dq.
-// TMEM: dQ^T chunks at columns 0, 64, 128, 192 (+256 for the rope rows), S at 320, dP at 384,
-// and three 64-column dKV^T buffers at 448, 320 and 384 (the last two reuse S and dP once the
-// math warps have read them).
+//                             drained into fp32 reductions on dkv
+// The fp32 reductions are the longest job (~2 k cycles per 128-row chunk), so they run on
+// warps of their own, out of two TMEM buffers of their own, fed by an MMA issuer of their own:
+// the next block's gather, S, dP, P / dS' and dQ proceed while the previous block drains.
+// Issuer B starts a block's dKV^T chunks once dQ^T of that block has run, so they fill the
+// tensor pipe while the next block is gathered instead of competing with S, dP and dQ^T.
+// Warp roles (512 threads, four warpgroups):
+//   warp 0        issuer A: S, dP, dQ^T (one thread); owns TMEM
+//   warps 1-3,13-15  gather: the block's kv rows with TMA gather4 (warp 1 also loads Q and dO)
+//   warps 4-7     math (TMEM lane quadrants 0-3): D / lse prologue, P and dS', dq epilogue
+//   warps 8-11    drain (lane quadrants 0-3): dKV^T chunks -> fp32 reductions on dkv
+//   warp 12       issuer B: dKV^T chunks (one thread)
+// setmaxnreg gives the math warpgroup 176 registers and the others 112.
+// TMEM: dQ^T chunks at columns 0, 64, 128, 192 (+256 for the rope rows); S and dP: with a rope
+// chunk one shared 64-column buffer at 320 (S first, dP once S has been read), otherwise S at
+// 256 and dP at 320; dKV^T buffers at 384 and 448.
 
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 512;
 constexpr int kBwdMathWarp0 = 4;
-constexpr int kBwdGatherWarps = 7;                 // warps 1, 2, 3, 8, 9, 10, 11
-constexpr uint32_t kBwdTmemS = 320, kBwdTmemDP = 384, kBwdTmemX0 = 448;
+constexpr int kBwdDrainWarp0 = 8;
+constexpr int kBwdIssuerB = 12;
+constexpr int kBwdGatherWarps = 6;                 // warps 1, 2, 3, 13, 14, 15
+constexpr int kBwdRowSlots = 4;                    // blocks whose row table may be live at once
+constexpr int kBwdMathRegs = 176;                  // 128 x 176 + 384 x 112 = 512 x 128
+constexpr int kBwdOtherRegs = 112;
+constexpr uint32_t kBwdTmemDP = 320, kBwdTmemX0 = 384, kBwdTmemX1 = 448;
 
 struct BwdParams {
   const int32_t* indices;      // [s_q, topk]
@@ -51,11 +65,6 @@ struct BwdParams {
   uint64_t wait_limit_ns;
 };
 
-__device__ __forceinline__ uint32_t bwd_dkv_col(int c) {
-  const int i = c % 3;
-  return i == 0 ? kBwdTmemX0 : (i == 1 ? kBwdTmemS : kBwdTmemDP);
-}
-
 // TMA row coordinate of slot j of row t (j < L): the kv row, or -1 when the slot does not count
 __device__ __forceinline__ int bwd_row(const BwdParams& p, const int32_t* idx_row, int j, int L) {
   if (j >= L) return -1;
@@ -71,6 +80,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int kQkSteps = D_QK / 16;
   constexpr int kDkvChunks = (D_QK + 127) / 128;     // 128-row chunks of d (the last may be 64)
   constexpr bool kRope = (D_QK % 128) != 0;
+  // with a rope chunk dQ^T takes columns 256..319 too, so S and dP share one buffer
+  constexpr uint32_t kTmemS = kRope ? kBwdTmemDP : 256u;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -80,10 +91,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sP = sKV + kChunks * 8192;                 // [64 heads][64 keys] bf16
   uint8_t* sDS = sP + 8192;                           // [64 heads][64 keys] bf16 (sm_scale dS)
 
-  __shared__ __align__(8) uint64_t bar_qdo_full, bar_kv_full, bar_kv_empty, bar_s_full, bar_p_full,
-      bar_tiles_free, bar_dq_full, bar_final;
-  __shared__ __align__(8) uint64_t bar_x_full[3], bar_x_free[3];
-  __shared__ int32_t s_rows[2][64];
+  __shared__ __align__(8) uint64_t bar_qdo_full, bar_kv_full, bar_kv_empty, bar_s_full, bar_s_free, bar_dp_full,
+      bar_p_full, bar_tiles_free, bar_dq_full, bar_final_a, bar_final_b;
+  __shared__ __align__(8) uint64_t bar_x_full[2], bar_x_free[2], bar_rows_full[kBwdRowSlots];
+  __shared__ int32_t s_rows[kBwdRowSlots][64];
   __shared__ float s_delta[64];
   __shared__ float s_lse2[64];
   __shared__ uint32_t tmem_slot;
@@ -107,14 +118,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&bar_kv_full), 1);
     mbar_init(smem_u32(&bar_kv_empty), 1);
     mbar_init(smem_u32(&bar_s_full), 1);
+    mbar_init(smem_u32(&bar_s_free), 4);
+    mbar_init(smem_u32(&bar_dp_full), 1);
     mbar_init(smem_u32(&bar_p_full), 128);
-    mbar_init(smem_u32(&bar_tiles_free), 1);
+    mbar_init(smem_u32(&bar_tiles_free), 2);          // dQ^T (issuer A) and dKV^T (issuer B)
     mbar_init(smem_u32(&bar_dq_full), 1);
-    mbar_init(smem_u32(&bar_final), 1);
-    for (int i = 0; i < 3; ++i) {
+    mbar_init(smem_u32(&bar_final_a), 1);
+    mbar_init(smem_u32(&bar_final_b), 1);
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_x_full[i]), 1);
       mbar_init(smem_u32(&bar_x_free[i]), 4);
     }
+    for (int i = 0; i < kBwdRowSlots; ++i) mbar_init(smem_u32(&bar_rows_full[i]), 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -127,95 +142,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = tmem_slot;
   const int64_t qrow = t * p.h_q + static_cast<int64_t>(g) * 64;   // first (token, head) row
 
-  if (warp == 0) {
-    // ======================================================== MMA issuer
-    if (lane == 0 && nb > 0) {
-      constexpr uint32_t id_s = make_idesc_bf16(64, 64, false, false);
-      constexpr uint32_t id_dq = make_idesc_bf16(128, 64, true, false);
-      constexpr uint32_t id_dq64 = make_idesc_bf16(64, 64, true, false);
-      constexpr uint32_t id_kv = make_idesc_bf16(128, 64, true, true);
-      constexpr uint32_t id_kv64 = make_idesc_bf16(64, 64, true, true);
-      const uint64_t q_k = make_sdesc_sw128(smem_u32(sQ), 16, 1024);      // Q, K-major
-      const uint64_t do_k = make_sdesc_sw128(smem_u32(sDO), 16, 1024);    // dO, K-major
-      const uint64_t kv_k = make_sdesc_sw128(smem_u32(sKV), 16, 1024);    // K / V rows, K-major
-      const uint64_t kv_mn = make_sdesc_sw128(smem_u32(sKV), 8192, 1024); // K^T, MN-major
-      const uint64_t q_mn = make_sdesc_sw128(smem_u32(sQ), 8192, 1024);   // Q^T, MN-major
-      const uint64_t do_mn = make_sdesc_sw128(smem_u32(sDO), 8192, 1024); // dO^T, MN-major
-      const uint64_t ds_k = make_sdesc_sw128(smem_u32(sDS), 16, 1024);    // dS'^T operand, K-major
-      const uint64_t ds_mn = make_sdesc_sw128(smem_u32(sDS), 8192, 1024); // dS' operand, MN-major
-      const uint64_t p_mn = make_sdesc_sw128(smem_u32(sP), 8192, 1024);   // P operand, MN-major
-      uint32_t xu[3] = {0u, 0u, 0u};                  // fills of each dKV^T buffer so far
-      wait_or_flag(smem_u32(&bar_qdo_full), 0, abort, lim);
-      for (int b = 0; b < nb && !*abort; ++b) {
-        wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);
-        SMLA_TRACE_EVENT(b, kTrGatherIssue);
-        // S and dP reuse the columns of dKV^T buffers 1 and 2: every drain of them is done
-        if (xu[1] > 0) wait_or_flag(smem_u32(&bar_x_free[1]), (xu[1] - 1) & 1, abort, lim);
-        if (xu[2] > 0) wait_or_flag(smem_u32(&bar_x_free[2]), (xu[2] - 1) & 1, abort, lim);
-        tc_fence_after();
-#pragma unroll 4
-        for (int ks = 0; ks < kQkSteps; ++ks) {
-          const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-          umma_ss(tmem + kBwdTmemS, q_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
-        }
-#pragma unroll 4
-        for (int ks = 0; ks < 32; ++ks) {
-          const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-          umma_ss(tmem + kBwdTmemDP, do_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&bar_s_full));
-        SMLA_TRACE_EVENT(b, kTrQkIssue);
-        wait_or_flag(smem_u32(&bar_p_full), b & 1, abort, lim);
-        tc_fence_after();
-        // dQ^T += K^T dS'^T over this block's 64 keys
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_ss(tmem + 64 * c, kv_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_dq,
-                    (b > 0 || ks > 0) ? 1u : 0u);
-        if constexpr (kRope) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_ss(tmem + 256, kv_mn + ((8 * 8192 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_dq64,
-                    (b > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&bar_kv_empty));          // S, dP and dQ^T have read the stage
-        SMLA_TRACE_EVENT(b, kTrPvIssue);
-        // dKV^T chunk c = Q^T dS' (+ dO^T P on the value rows), one buffer of three each
-#pragma unroll
-        for (int c = 0; c < kDkvChunks; ++c) {
-          const int i = c % 3;
-          if (xu[i] > 0) wait_or_flag(smem_u32(&bar_x_free[i]), (xu[i] - 1) & 1, abort, lim);
-          tc_fence_after();
-          const uint32_t col = tmem + bwd_dkv_col(c);
-          if (!kRope || c < 4) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_ss(col, q_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv,
-                      ks > 0 ? 1u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_ss(col, do_mn + ((2 * c * 8192 + ks * 2048) >> 4), p_mn + ((ks * 2048) >> 4), id_kv, 1u);
-          } else {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_ss(col, q_mn + ((8 * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv64,
-                      ks > 0 ? 1u : 0u);
-          }
-          umma_commit(smem_u32(&bar_x_full[i]));
-          ++xu[i];
-        }
-        umma_commit(smem_u32(&bar_tiles_free));        // P and dS' tiles may be rewritten
-        SMLA_TRACE_EVENT(b, kTrEpilogue);
-      }
-      umma_commit(smem_u32(&bar_dq_full));
-      umma_commit(smem_u32(&bar_final));
-      wait_drain(smem_u32(&bar_final), 0, lim);
-    }
-    __syncwarp();
-  } else if (warp >= kBwdMathWarp0 && warp < kBwdMathWarp0 + 4) {
-    // ======================================================== P / dS', dKV^T drains, dq
+  if (warp >= kBwdMathWarp0 && warp < kBwdMathWarp0 + 4) {
+    reg_alloc<kBwdMathRegs>();
+    // ======================================================== math (see below)
+    // P / dS' per block and the dq epilogue of the item
     const int q = warp - kBwdMathWarp0;
     const int mt = tid - kBwdMathWarp0 * 32;         // 0..127
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -260,27 +190,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float c2 = p.sm_scale * kLog2e;
     const float dA = s_delta[hA], dB = s_delta[hB];
     const float lA = s_lse2[hA], lB = s_lse2[hB];
-    uint32_t xu[3] = {0u, 0u, 0u};
     for (int b = 0; b < nb && !*abort; ++b) {
-      const int sb = b & 1;
-      wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);   // also publishes s_rows[sb]
+      const int rs = b % kBwdRowSlots;
+      wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);   // also publishes s_rows[rs]
       wait_or_flag(smem_u32(&bar_s_full), b & 1, abort, lim);
       SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrSReady);
       tc_fence_after();
       float sv[32], dv[32];
 #pragma unroll
       for (int i8 = 0; i8 < 8; ++i8) {
-        uint32_t r4[4], d4[4];
-        tmem_ld_16x256b(tmem + lane_base + kBwdTmemS + 8 * i8, r4);
+        uint32_t r4[4];
+        tmem_ld_16x256b(tmem + lane_base + kTmemS + 8 * i8, r4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sv[4 * i8 + e] = __uint_as_float(r4[e]);
+      }
+      if constexpr (kRope) {
+        // S is in registers: its columns take dP next
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
+        wait_or_flag(smem_u32(&bar_dp_full), b & 1, abort, lim);
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int i8 = 0; i8 < 8; ++i8) {
+        uint32_t d4[4];
         tmem_ld_16x256b(tmem + lane_base + kBwdTmemDP + 8 * i8, d4);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sv[4 * i8 + e] = __uint_as_float(r4[e]);
-          dv[4 * i8 + e] = __uint_as_float(d4[e]);
-        }
+        for (int e = 0; e < 4; ++e) dv[4 * i8 + e] = __uint_as_float(d4[e]);
       }
       tmem_ld_wait();
-      // the previous block's P / dS' tiles have been read by every MMA
+      // the previous block's P / dS' tiles have been read by every MMA (dQ^T and dKV^T)
       if (b >= 1) wait_or_flag(smem_u32(&bar_tiles_free), (b - 1) & 1, abort, lim);
       const int swA = hA & 7, swB = hB & 7;
 #pragma unroll
@@ -288,7 +229,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float pa[2], pb[2], da[2], db[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const bool ok = s_rows[sb][8 * i8 + cpair + e] >= 0;
+          const bool ok = s_rows[rs][8 * i8 + cpair + e] >= 0;
           pa[e] = ok ? fast_exp2(fmaf(sv[4 * i8 + e], c2, -lA)) : 0.f;
           pb[e] = ok ? fast_exp2(fmaf(sv[4 * i8 + 2 + e], c2, -lB)) : 0.f;
           da[e] = p.sm_scale * pa[e] * (dv[4 * i8 + e] - dA);
@@ -302,44 +243,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p_full));
+      mbar_arrive(smem_u32(&bar_p_full));            // also: S and dP have been read
       SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, b, kTrPReady);
-      // drain this block's dKV^T chunks into fp32 reductions on the selected kv rows
-#pragma unroll
-      for (int c = 0; c < kDkvChunks; ++c) {
-        const int i = c % 3;
-        wait_or_flag(smem_u32(&bar_x_full[i]), xu[i] & 1, abort, lim);
-        SMLA_TRACE_EVENT_IF(c == 0 && q == 0 && lane == 0, b, kTrSLoaded);
-        ++xu[i];
-        tc_fence_after();
-        const bool rope = kRope && c == 4;
-        const int d = rope ? 512 + 16 * q + lane : 128 * c + 32 * q + lane;
-        float* base = p.dkv + d;
-        // two halves of 32 keys; the buffer goes back once both are in registers
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32];
-          tmem_ld16(tmem + lane_base + bwd_dkv_col(c) + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-          tmem_ld16(tmem + lane_base + bwd_dkv_col(c) + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-          tmem_ld_wait();
-          if (half == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bar_x_free[i]));
-          }
-          if (!rope || lane < 16) {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int row = s_rows[sb][32 * half + k];
-              if (row >= 0) atomicAdd(base + static_cast<int64_t>(row) * D_QK, __uint_as_float(v[k]));
-            }
-          }
-        }
-      }
     }
-    // ---- dq of this item: dQ^T chunk c holds rows d, columns = heads (the last block's drains
-    // end here)
-    SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, nb, kTrSent);
+    // ---- dq of this item: dQ^T chunk c holds rows d, columns = heads
     float* dq = p.dq + qrow * D_QK;
     if (nb > 0) {
       wait_or_flag(smem_u32(&bar_dq_full), 0, abort, lim);
@@ -366,38 +273,217 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    // ======================================================== gather (warps 1-3, 8-11)
-    const int gw = warp < 4 ? warp - 1 : warp - 5;   // 0..6
-    const bool leader = (gw == 0 && lane == 0);
-    if (leader && nb > 0) {
-      mbar_arrive_expect_tx(smem_u32(&bar_qdo_full), (kChunks + 8) * 8192u);
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
-      for (int c = 0; c < 8; ++c)
-        tma_load_2d(smem_u32(sDO + c * 8192), &do_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
-    }
-    const int it = gw + kBwdGatherWarps * lane;       // (4-row group, chunk) item of a block
-    const int grp = it & 15, chunk = it >> 4;
-    for (int b = 0; b < nb && !*abort; ++b) {
-      if (b >= 1) wait_or_flag(smem_u32(&bar_kv_empty), (b - 1) & 1, abort, lim);
-      SMLA_TRACE_EVENT_IF(leader, b, kTrRing);
-      if (gw == 0) {
-        s_rows[b & 1][lane] = bwd_row(p, idx_row, 64 * b + lane, L);
-        s_rows[b & 1][lane + 32] = bwd_row(p, idx_row, 64 * b + lane + 32, L);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bar_kv_full), kChunks * 8192u);
+    reg_dealloc<kBwdOtherRegs>();
+    if (warp == 0) {
+      // ======================================================== issuer A: S, dP, dQ^T
+      if (lane == 0 && nb > 0) {
+        constexpr uint32_t id_s = make_idesc_bf16(64, 64, false, false);
+        constexpr uint32_t id_dq = make_idesc_bf16(128, 64, true, false);
+        constexpr uint32_t id_dq64 = make_idesc_bf16(64, 64, true, false);
+        const uint64_t q_k = make_sdesc_sw128(smem_u32(sQ), 16, 1024);      // Q, K-major
+        const uint64_t do_k = make_sdesc_sw128(smem_u32(sDO), 16, 1024);    // dO, K-major
+        const uint64_t kv_k = make_sdesc_sw128(smem_u32(sKV), 16, 1024);    // K / V rows, K-major
+        const uint64_t kv_mn = make_sdesc_sw128(smem_u32(sKV), 8192, 1024); // K^T, MN-major
+        const uint64_t ds_k = make_sdesc_sw128(smem_u32(sDS), 16, 1024);    // dS'^T operand, K-major
+        wait_or_flag(smem_u32(&bar_qdo_full), 0, abort, lim);
+        for (int b = 0; b < nb && !*abort; ++b) {
+          wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);
+          SMLA_TRACE_EVENT(b, kTrGatherIssue);
+          tc_fence_after();
+          // S and dP: their columns were read by the math warps before p_full(b-1), which this
+          // thread waited for before dQ^T(b-1)
+#pragma unroll 4
+          for (int ks = 0; ks < kQkSteps; ++ks) {
+            const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+            umma_ss(tmem + kTmemS, q_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
+          }
+          if constexpr (kRope) {
+            umma_commit(smem_u32(&bar_s_full));
+            wait_or_flag(smem_u32(&bar_s_free), b & 1, abort, lim);   // S is in registers
+            tc_fence_after();
+          }
+#pragma unroll 4
+          for (int ks = 0; ks < 32; ++ks) {
+            const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+            umma_ss(tmem + kBwdTmemDP, do_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(kRope ? &bar_dp_full : &bar_s_full));
+          SMLA_TRACE_EVENT(b, kTrQkIssue);
+          wait_or_flag(smem_u32(&bar_p_full), b & 1, abort, lim);
+          tc_fence_after();
+          // dQ^T += K^T dS'^T over this block's 64 keys
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_ss(tmem + 64 * c, kv_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_dq,
+                      (b > 0 || ks > 0) ? 1u : 0u);
+          if constexpr (kRope) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_ss(tmem + 256, kv_mn + ((8 * 8192 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_dq64,
+                      (b > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&bar_kv_empty));          // S, dP and dQ^T have read the stage
+          umma_commit(smem_u32(&bar_tiles_free));        // ... and dQ^T the dS' tile
+          SMLA_TRACE_EVENT(b, kTrPvIssue);
+        }
+        umma_commit(smem_u32(&bar_dq_full));
+        umma_commit(smem_u32(&bar_final_a));
+        wait_drain(smem_u32(&bar_final_a), 0, lim);
       }
-      if (it < 16 * kChunks) {
+      __syncwarp();
+    } else if (warp == kBwdIssuerB) {
+      // ======================================================== issuer B: dKV^T chunks
+      if (lane == 0 && nb > 0) {
+        constexpr uint32_t id_kv = make_idesc_bf16(128, 64, true, true);
+        constexpr uint32_t id_kv64 = make_idesc_bf16(64, 64, true, true);
+        const uint64_t q_mn = make_sdesc_sw128(smem_u32(sQ), 8192, 1024);   // Q^T, MN-major
+        const uint64_t do_mn = make_sdesc_sw128(smem_u32(sDO), 8192, 1024); // dO^T, MN-major
+        const uint64_t ds_mn = make_sdesc_sw128(smem_u32(sDS), 8192, 1024); // dS' operand, MN-major
+        const uint64_t p_mn = make_sdesc_sw128(smem_u32(sP), 8192, 1024);   // P operand, MN-major
+        uint32_t xu[2] = {0u, 0u};                    // fills of each dKV^T buffer so far
+        wait_or_flag(smem_u32(&bar_qdo_full), 0, abort, lim);
+        for (int b = 0; b < nb && !*abort; ++b) {
+          // after dQ^T(b) (issuer A's critical chain) has run: dKV^T(b) then fills the tensor
+          // pipe while block b+1 is gathered
+          wait_or_flag(smem_u32(&bar_kv_empty), b & 1, abort, lim);
+#pragma unroll
+          for (int c = 0; c < kDkvChunks; ++c) {
+            const int i = c & 1;
+            if (xu[i] > 0) wait_or_flag(smem_u32(&bar_x_free[i]), (xu[i] - 1) & 1, abort, lim);
+            tc_fence_after();
+            const uint32_t col = tmem + (i ? kBwdTmemX1 : kBwdTmemX0);
+            if (!kRope || c < 4) {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                umma_ss(col, q_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv,
+                        ks > 0 ? 1u : 0u);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                umma_ss(col, do_mn + ((2 * c * 8192 + ks * 2048) >> 4), p_mn + ((ks * 2048) >> 4), id_kv, 1u);
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                umma_ss(col, q_mn + ((8 * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv64,
+                        ks > 0 ? 1u : 0u);
+            }
+            umma_commit(smem_u32(&bar_x_full[i]));
+            ++xu[i];
+          }
+          umma_commit(smem_u32(&bar_tiles_free));        // P and dS' tiles may be rewritten
+          SMLA_TRACE_EVENT(b, kTrEpilogue);
+        }
+        umma_commit(smem_u32(&bar_final_b));
+        wait_drain(smem_u32(&bar_final_b), 0, lim);
+      }
+      __syncwarp();
+    } else if (warp >= kBwdDrainWarp0 && warp < kBwdDrainWarp0 + 4) {
+      // ======================================================== drain (see below)
+      // dKV^T chunks of every block, in issue order, into fp32 reductions on the selected rows.
+      // Warp 8+q owns TMEM lanes 32q..32q+31: d = 128c + 32q + lane (or 512 + 16q + lane, lanes
+      // 0-15, for the 64 rope rows), and the 32 lanes of a warp cover 128 contiguous bytes of one
+      // kv row.
+      const int q = warp - kBwdDrainWarp0;
+      const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+      uint32_t xu[2] = {0u, 0u};
+      for (int b = 0; b < nb && !*abort; ++b) {
+        const int rs = b % kBwdRowSlots;
+        // the block's row table (written by the first gather warp before its gathers)
+        wait_or_flag(smem_u32(&bar_rows_full[rs]), (b / kBwdRowSlots) & 1, abort, lim);
+#pragma unroll
+        for (int c = 0; c < kDkvChunks; ++c) {
+          const int i = c & 1;
+          wait_or_flag(smem_u32(&bar_x_full[i]), xu[i] & 1, abort, lim);
+          SMLA_TRACE_EVENT_IF(c == 0 && q == 0 && lane == 0, b, kTrSLoaded);
+          ++xu[i];
+          tc_fence_after();
+          const bool rope = kRope && c == 4;
+          const int d = rope ? 512 + 16 * q + lane : 128 * c + 32 * q + lane;
+          float* base = p.dkv + d;
+          const uint32_t col = i ? kBwdTmemX1 : kBwdTmemX0;
+          // two halves of 32 keys; the buffer goes back once both are in registers
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[32];
+            tmem_ld16(tmem + lane_base + col + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+            tmem_ld16(tmem + lane_base + col + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+            tmem_ld_wait();
+            if (half == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&bar_x_free[i]));
+            }
+            if (!rope || lane < 16) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const int row = s_rows[rs][32 * half + k];
+                if (row >= 0) atomicAdd(base + static_cast<int64_t>(row) * D_QK, __uint_as_float(v[k]));
+              }
+            }
+          }
+        }
+      }
+      SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, nb, kTrSent);
+    } else {
+      // ======================================================== gather (see below)
+      // warps 1-3 and 13-15; the first loads the item's Q and dO tiles and publishes each block's
+      // row table (TMA row coordinates, -1 for slots that do not count)
+      const int gw = warp < 4 ? warp - 1 : warp - 10;   // 0..5
+      const bool leader = (gw == 0 && lane == 0);
+      if (leader && nb > 0) {
+        mbar_arrive_expect_tx(smem_u32(&bar_qdo_full), (kChunks + 8) * 8192u);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
+        for (int c = 0; c < 8; ++c)
+          tma_load_2d(smem_u32(sDO + c * 8192), &do_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
+      }
+      const int it = gw + kBwdGatherWarps * lane;       // (4-row group, chunk) item of a block
+      const int grp = it & 15, chunk = it >> 4;
+      const bool issues = it < 16 * kChunks;
+      // the rows of block b+1 are loaded while block b is in flight (indices come from HBM)
+      auto rows4 = [&](int b) {
         const int j = 64 * b + 4 * grp;
-        tma_gather4(smem_u32(sKV + chunk * 8192 + grp * 512), &kv_map, 64 * chunk, bwd_row(p, idx_row, j, L),
-                    bwd_row(p, idx_row, j + 1, L), bwd_row(p, idx_row, j + 2, L), bwd_row(p, idx_row, j + 3, L),
-                    smem_u32(&bar_kv_full));
+        return make_int4(bwd_row(p, idx_row, j, L), bwd_row(p, idx_row, j + 1, L), bwd_row(p, idx_row, j + 2, L),
+                         bwd_row(p, idx_row, j + 3, L));
+      };
+      auto rows2 = [&](int b) {
+        return make_int2(bwd_row(p, idx_row, 64 * b + lane, L), bwd_row(p, idx_row, 64 * b + lane + 32, L));
+      };
+      int4 nxt4 = make_int4(-1, -1, -1, -1);
+      int2 nxt2 = make_int2(-1, -1);
+      if (nb > 0) {
+        if (issues) nxt4 = rows4(0);
+        if (gw == 0) nxt2 = rows2(0);
       }
-    }
-    // the Q / dO tiles and the last block have landed before this CTA may exit
-    if (leader && nb > 0) {
-      wait_drain(smem_u32(&bar_qdo_full), 0, lim);
-      wait_drain(smem_u32(&bar_kv_full), (nb - 1) & 1, lim);
+      for (int b = 0; b < nb && !*abort; ++b) {
+        const int4 cur4 = nxt4;
+        const int2 cur2 = nxt2;
+        if (b + 1 < nb) {
+          if (issues) nxt4 = rows4(b + 1);
+          if (gw == 0) nxt2 = rows2(b + 1);
+        }
+        if (b >= 1) wait_or_flag(smem_u32(&bar_kv_empty), (b - 1) & 1, abort, lim);
+        SMLA_TRACE_EVENT_IF(leader, b, kTrRing);
+        if (gw == 0) {
+          const int rs = b % kBwdRowSlots;
+          s_rows[rs][lane] = cur2.x;
+          s_rows[rs][lane + 32] = cur2.y;
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&bar_rows_full[rs]));
+            mbar_arrive_expect_tx(smem_u32(&bar_kv_full), kChunks * 8192u);
+          }
+        }
+        if (issues)
+          tma_gather4(smem_u32(sKV + chunk * 8192 + grp * 512), &kv_map, 64 * chunk, cur4.x, cur4.y, cur4.z, cur4.w,
+                      smem_u32(&bar_kv_full));
+      }
+      // the Q / dO tiles and the last block have landed before this CTA may exit
+      if (leader && nb > 0) {
+        wait_drain(smem_u32(&bar_qdo_full), 0, lim);
+        wait_drain(smem_u32(&bar_kv_full), (nb - 1) & 1, lim);
+      }
     }
   }
 
