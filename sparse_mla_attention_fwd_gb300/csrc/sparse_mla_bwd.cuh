@@ -21,7 +21,7 @@
 //   dKV^T [d x 64 keys]     = Q^T dS' + dO^T P    (per 128-row chunk of d, K=64 heads; TMEM),
 //                             drained into fp32 reductions on dkv
 // The fp32 reductions are the longest job (~2 k cycles per 128-row chunk), so they run on
-// warps of their own, out of two TMEM buffers of their own, fed by an MMA issuer of their own:
+// warps of their own, out of a TMEM buffer of their own, fed by an MMA issuer of their own:
 // the next block's gather, S, dP, P / dS' and dQ proceed while the previous block drains.
 // Issuer B starts a block's dKV^T chunks once dQ^T of that block has run, so they fill the
 // tensor pipe while the next block is gathered instead of competing with S, dP and dQ^T.
@@ -32,9 +32,10 @@
 //   warps 8-11    drain (lane quadrants 0-3): dKV^T chunks -> fp32 reductions on dkv
 //   warp 12       issuer B: dKV^T chunks (one thread)
 // setmaxnreg gives the math warpgroup 176 registers and the others 112.
-// TMEM: dQ^T chunks at columns 0, 64, 128, 192 (+256 for the rope rows); S and dP: with a rope
-// chunk one shared 64-column buffer at 320 (S first, dP once S has been read), otherwise S at
-// 256 and dP at 320; dKV^T buffers at 384 and 448.
+// TMEM: dQ^T chunks at columns 0, 64, 128, 192 (+256 for the rope rows); S at 320, dP at 384
+// and the dKV^T buffer at 448.  One dKV^T buffer is enough: the drain warps hand it back as soon
+// as a chunk is in their registers, long before its reductions end, and the columns it frees let
+// S and dP have buffers of their own, so dP does not wait for S to be read.
 
 constexpr int kBwdThreads = 512;
 constexpr int kBwdMathWarp0 = 4;
@@ -44,7 +45,7 @@ constexpr int kBwdGatherWarps = 6;                 // warps 1, 2, 3, 13, 14, 15
 constexpr int kBwdRowSlots = 4;                    // blocks whose row table may be live at once
 constexpr int kBwdMathRegs = 176;                  // 128 x 176 + 384 x 112 = 512 x 128
 constexpr int kBwdOtherRegs = 112;
-constexpr uint32_t kBwdTmemDP = 320, kBwdTmemX0 = 384, kBwdTmemX1 = 448;
+constexpr uint32_t kBwdTmemS = 320, kBwdTmemDP = 384, kBwdTmemX = 448;
 
 struct BwdParams {
   const int32_t* indices;      // [s_q, topk]
@@ -80,8 +81,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int kQkSteps = D_QK / 16;
   constexpr int kDkvChunks = (D_QK + 127) / 128;     // 128-row chunks of d (the last may be 64)
   constexpr bool kRope = (D_QK % 128) != 0;
-  // with a rope chunk dQ^T takes columns 256..319 too, so S and dP share one buffer
-  constexpr uint32_t kTmemS = kRope ? kBwdTmemDP : 256u;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -91,9 +90,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sP = sKV + kChunks * 8192;                 // [64 heads][64 keys] bf16
   uint8_t* sDS = sP + 8192;                           // [64 heads][64 keys] bf16 (sm_scale dS)
 
-  __shared__ __align__(8) uint64_t bar_qdo_full, bar_kv_full, bar_kv_empty, bar_s_full, bar_s_free, bar_dp_full,
+  __shared__ __align__(8) uint64_t bar_qdo_full, bar_kv_full, bar_kv_empty, bar_s_full,
       bar_p_full, bar_tiles_free, bar_dq_full, bar_final_a, bar_final_b;
-  __shared__ __align__(8) uint64_t bar_x_full[2], bar_x_free[2], bar_rows_full[kBwdRowSlots];
+  __shared__ __align__(8) uint64_t bar_x_full, bar_x_free, bar_rows_full[kBwdRowSlots];
   __shared__ int32_t s_rows[kBwdRowSlots][64];
   __shared__ float s_delta[64];
   __shared__ float s_lse2[64];
@@ -118,17 +117,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&bar_kv_full), 1);
     mbar_init(smem_u32(&bar_kv_empty), 1);
     mbar_init(smem_u32(&bar_s_full), 1);
-    mbar_init(smem_u32(&bar_s_free), 4);
-    mbar_init(smem_u32(&bar_dp_full), 1);
     mbar_init(smem_u32(&bar_p_full), 128);
     mbar_init(smem_u32(&bar_tiles_free), 2);          // dQ^T (issuer A) and dKV^T (issuer B)
     mbar_init(smem_u32(&bar_dq_full), 1);
     mbar_init(smem_u32(&bar_final_a), 1);
     mbar_init(smem_u32(&bar_final_b), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_x_full[i]), 1);
-      mbar_init(smem_u32(&bar_x_free[i]), 4);
-    }
+    mbar_init(smem_u32(&bar_x_full), 1);
+    mbar_init(smem_u32(&bar_x_free), 4);
     for (int i = 0; i < kBwdRowSlots; ++i) mbar_init(smem_u32(&bar_rows_full[i]), 1);
     fence_mbar_init();
   }
@@ -200,18 +195,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int i8 = 0; i8 < 8; ++i8) {
         uint32_t r4[4];
-        tmem_ld_16x256b(tmem + lane_base + kTmemS + 8 * i8, r4);
+        tmem_ld_16x256b(tmem + lane_base + kBwdTmemS + 8 * i8, r4);
 #pragma unroll
         for (int e = 0; e < 4; ++e) sv[4 * i8 + e] = __uint_as_float(r4[e]);
-      }
-      if constexpr (kRope) {
-        // S is in registers: its columns take dP next
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
-        wait_or_flag(smem_u32(&bar_dp_full), b & 1, abort, lim);
-        tc_fence_after();
       }
 #pragma unroll
       for (int i8 = 0; i8 < 8; ++i8) {
@@ -295,19 +281,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 4
           for (int ks = 0; ks < kQkSteps; ++ks) {
             const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-            umma_ss(tmem + kTmemS, q_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
-          }
-          if constexpr (kRope) {
-            umma_commit(smem_u32(&bar_s_full));
-            wait_or_flag(smem_u32(&bar_s_free), b & 1, abort, lim);   // S is in registers
-            tc_fence_after();
+            umma_ss(tmem + kBwdTmemS, q_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
           }
 #pragma unroll 4
           for (int ks = 0; ks < 32; ++ks) {
             const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
             umma_ss(tmem + kBwdTmemDP, do_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(kRope ? &bar_dp_full : &bar_s_full));
+          umma_commit(smem_u32(&bar_s_full));              // S and dP
           SMLA_TRACE_EVENT(b, kTrQkIssue);
           wait_or_flag(smem_u32(&bar_p_full), b & 1, abort, lim);
           tc_fence_after();
@@ -342,7 +323,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t do_mn = make_sdesc_sw128(smem_u32(sDO), 8192, 1024); // dO^T, MN-major
         const uint64_t ds_mn = make_sdesc_sw128(smem_u32(sDS), 8192, 1024); // dS' operand, MN-major
         const uint64_t p_mn = make_sdesc_sw128(smem_u32(sP), 8192, 1024);   // P operand, MN-major
-        uint32_t xu[2] = {0u, 0u};                    // fills of each dKV^T buffer so far
+        uint32_t xu = 0;                              // fills of the dKV^T buffer so far
         wait_or_flag(smem_u32(&bar_qdo_full), 0, abort, lim);
         for (int b = 0; b < nb && !*abort; ++b) {
           // after dQ^T(b) (issuer A's critical chain) has run: dKV^T(b) then fills the tensor
@@ -350,10 +331,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           wait_or_flag(smem_u32(&bar_kv_empty), b & 1, abort, lim);
 #pragma unroll
           for (int c = 0; c < kDkvChunks; ++c) {
-            const int i = c & 1;
-            if (xu[i] > 0) wait_or_flag(smem_u32(&bar_x_free[i]), (xu[i] - 1) & 1, abort, lim);
+            if (xu > 0) wait_or_flag(smem_u32(&bar_x_free), (xu - 1) & 1, abort, lim);
             tc_fence_after();
-            const uint32_t col = tmem + (i ? kBwdTmemX1 : kBwdTmemX0);
+            const uint32_t col = tmem + kBwdTmemX;
             if (!kRope || c < 4) {
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
@@ -368,8 +348,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 umma_ss(col, q_mn + ((8 * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv64,
                         ks > 0 ? 1u : 0u);
             }
-            umma_commit(smem_u32(&bar_x_full[i]));
-            ++xu[i];
+            umma_commit(smem_u32(&bar_x_full));
+            ++xu;
           }
           umma_commit(smem_u32(&bar_tiles_free));        // P and dS' tiles may be rewritten
           SMLA_TRACE_EVENT(b, kTrEpilogue);
@@ -386,22 +366,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // kv row.
       const int q = warp - kBwdDrainWarp0;
       const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-      uint32_t xu[2] = {0u, 0u};
+      uint32_t xu = 0;
       for (int b = 0; b < nb && !*abort; ++b) {
         const int rs = b % kBwdRowSlots;
         // the block's row table (written by the first gather warp before its gathers)
         wait_or_flag(smem_u32(&bar_rows_full[rs]), (b / kBwdRowSlots) & 1, abort, lim);
 #pragma unroll
         for (int c = 0; c < kDkvChunks; ++c) {
-          const int i = c & 1;
-          wait_or_flag(smem_u32(&bar_x_full[i]), xu[i] & 1, abort, lim);
+          wait_or_flag(smem_u32(&bar_x_full), xu & 1, abort, lim);
           SMLA_TRACE_EVENT_IF(c == 0 && q == 0 && lane == 0, b, kTrSLoaded);
-          ++xu[i];
+          ++xu;
           tc_fence_after();
           const bool rope = kRope && c == 4;
           const int d = rope ? 512 + 16 * q + lane : 128 * c + 32 * q + lane;
           float* base = p.dkv + d;
-          const uint32_t col = i ? kBwdTmemX1 : kBwdTmemX0;
+          const uint32_t col = kBwdTmemX;
           // two halves of 32 keys; the buffer goes back once both are in registers
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
@@ -412,7 +391,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (half == 1) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(&bar_x_free[i]));
+              if (lane == 0) mbar_arrive(smem_u32(&bar_x_free));
             }
             if (!rope || lane < 16) {
 #pragma unroll
@@ -466,6 +445,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (b >= 1) wait_or_flag(smem_u32(&bar_kv_empty), (b - 1) & 1, abort, lim);
         SMLA_TRACE_EVENT_IF(leader, b, kTrRing);
         if (gw == 0) {
+          // slot b % 4 was last read by the drains of block b-4: each drain warp ends them before
+          // it takes block b-3's first chunk, so the dKV^T buffer could not take block b-3's
+          // second chunk, nor dKV^T(b-2) run, nor the P / dS' tiles of block b-1 be written (the
+          // kv_empty(b-1) wait above follows those) before they were done
           const int rs = b % kBwdRowSlots;
           s_rows[rs][lane] = cur2.x;
           s_rows[rs][lane + 32] = cur2.y;
