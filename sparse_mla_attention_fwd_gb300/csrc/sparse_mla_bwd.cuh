@@ -13,38 +13,49 @@
 // lse is the forward's (natural log, sink excluded) and O the forward's bf16 output.
 //
 // Work item = (token, group of 64 heads), one CTA each.  Per 64-key block of the row:
-//   S   [64 heads x 64 keys] = Q K^T              (M=64, N=64, K=d_qk; TMEM)
-//   dP  [64 heads x 64 keys] = dO V^T             (M=64, N=64, K=512; TMEM)
-//   P, dS' = sm_scale P (dP - D)  -> shared memory as bf16 [heads][keys] (SW128)
+//   [S^T | dP^T] [64 keys x (64 + 64)] = K [Q; dO]^T   (M=64, N=128, K=512; then the rope
+//                             columns add K_rope Q_rope^T to S^T alone with N=64; TMEM)
+//   P^T, dS'^T = sm_scale P (dP - D)  -> shared memory as bf16 [keys][heads] (SW128)
 //   dQ^T [d_qk x 64 heads] += K^T dS'^T           (M=128 (+64 for the rope), N=64, K=64 keys;
 //                                                  TMEM, accumulated over the row's blocks)
 //   dKV^T [d x 64 keys]     = Q^T dS' + dO^T P    (per 128-row chunk of d, K=64 heads; TMEM),
 //                             drained into fp32 reductions on dkv
-// The fp32 reductions are the longest job (~2 k cycles per 128-row chunk), so they run on
-// warps of their own, out of a TMEM buffer of their own, fed by an MMA issuer of their own:
-// the next block's gather, S, dP, P / dS' and dQ proceed while the previous block drains.
-// Issuer B starts a block's dKV^T chunks once dQ^T of that block has run, so they fill the
-// tensor pipe while the next block is gathered instead of competing with S, dP and dQ^T.
-// Warp roles (512 threads, four warpgroups):
-//   warp 0        issuer A: S, dP, dQ^T (one thread); owns TMEM
-//   warps 1-3,13-15  gather: the block's kv rows with TMA gather4 (warp 1 also loads Q and dO)
+// A tcgen05.mma costs about the same time for N = 64 as for N = 128, so S and dP, which share
+// their B rows (the block's kv rows), run as one N = 128 product with the keys as M: half the
+// instructions of two M=64 x N=64 products.  With keys on TMEM lanes, each math thread holds two
+// keys and sixteen heads, and the masking of invalid slots is per lane.
+// The fp32 reductions are the longest job and set the block period, so they run on eight warps
+// of their own (two per TMEM lane quadrant, 32 keys each: more reductions in flight), out of a
+// TMEM buffer of their own, fed by an MMA issuer of their own: the next block's gather, S, dP,
+// P / dS' and dQ proceed while the previous block drains.  Issuer B starts a block's dKV^T
+// chunks once dQ^T of that block has run, so they fill the tensor pipe while the next block is
+// gathered instead of competing with S, dP and dQ^T.
+// With the reductions off the chain, the gather of the next block (which may start only once
+// dQ^T has read the single kv stage) is the longest step left on it; TMA issue throughput grows
+// with the number of issuing warps, so ten warps gather.
+// Warp roles (768 threads, six warpgroups):
+//   warp 0        issuer A: S^T / dP^T, dQ^T (one thread); owns TMEM
+//   warps 1-2, 16-23  gather: the block's kv rows with TMA gather4 (warp 1 also loads Q and dO
+//                 and publishes the row table)
+//   warp 3        issuer B: dKV^T chunks (one thread)
 //   warps 4-7     math (TMEM lane quadrants 0-3): D / lse prologue, P and dS', dq epilogue
-//   warps 8-11    drain (lane quadrants 0-3): dKV^T chunks -> fp32 reductions on dkv
-//   warp 12       issuer B: dKV^T chunks (one thread)
-// setmaxnreg gives the math warpgroup 176 registers and the others 112.
+//   warps 8-15    drain (lane quadrant warp % 4, keys 32 ((warp - 8) / 4) + 0..31): dKV^T
+//                 chunks -> fp32 reductions on dkv
+// 768 threads launch with 80 registers each; setmaxnreg gives the math warpgroup 120 and the
+// others 72, which uses the launch's 61440 registers exactly.
 // TMEM: dQ^T chunks at columns 0, 64, 128, 192 (+256 for the rope rows); S at 320, dP at 384
 // and the dKV^T buffer at 448.  One dKV^T buffer is enough: the drain warps hand it back as soon
 // as a chunk is in their registers, long before its reductions end, and the columns it frees let
 // S and dP have buffers of their own, so dP does not wait for S to be read.
 
-constexpr int kBwdThreads = 512;
+constexpr int kBwdThreads = 768;
 constexpr int kBwdMathWarp0 = 4;
 constexpr int kBwdDrainWarp0 = 8;
-constexpr int kBwdIssuerB = 12;
-constexpr int kBwdGatherWarps = 6;                 // warps 1, 2, 3, 13, 14, 15
+constexpr int kBwdIssuerB = 3;
+constexpr int kBwdGatherWarps = 10;                // warps 1, 2, 16-23
 constexpr int kBwdRowSlots = 4;                    // blocks whose row table may be live at once
-constexpr int kBwdMathRegs = 176;                  // 128 x 176 + 384 x 112 = 512 x 128
-constexpr int kBwdOtherRegs = 112;
+constexpr int kBwdMathRegs = 120;                  // 128 x 120 + 640 x 72 = 61440 = 768 x 80
+constexpr int kBwdOtherRegs = 72;
 constexpr uint32_t kBwdTmemS = 320, kBwdTmemDP = 384, kBwdTmemX = 448;
 
 struct BwdParams {
@@ -84,11 +95,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sQ = smem;                                 // [64 heads][D_QK], kChunks x 8 KB
-  uint8_t* sDO = sQ + kChunks * 8192;                 // [64 heads][512], 8 x 8 KB
-  uint8_t* sKV = sDO + 8 * 8192;                      // [64 keys][D_QK], kChunks x 8 KB
-  uint8_t* sP = sKV + kChunks * 8192;                 // [64 heads][64 keys] bf16
-  uint8_t* sDS = sP + 8192;                           // [64 heads][64 keys] bf16 (sm_scale dS)
+  // column chunk c (64 columns) of Q and of dO side by side: Q rows at sQD + 16 KB c, dO rows
+  // 8 KB further (the rope chunk c = 8 holds Q rows only), so that the 128 rows [Q; dO] of a
+  // chunk form one K-major operand
+  uint8_t* sQD = smem;
+  uint8_t* sKV = sQD + kChunks * 8192 + 8 * 8192;     // [64 keys][D_QK], kChunks x 8 KB
+  uint8_t* sP = sKV + kChunks * 8192;                 // [64 keys][64 heads] bf16
+  uint8_t* sDS = sP + 8192;                           // [64 keys][64 heads] bf16 (sm_scale dS)
 
   __shared__ __align__(8) uint64_t bar_qdo_full, bar_kv_full, bar_kv_empty, bar_s_full,
       bar_p_full, bar_tiles_free, bar_dq_full, bar_final_a, bar_final_b;
@@ -123,7 +136,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&bar_final_a), 1);
     mbar_init(smem_u32(&bar_final_b), 1);
     mbar_init(smem_u32(&bar_x_full), 1);
-    mbar_init(smem_u32(&bar_x_free), 4);
+    mbar_init(smem_u32(&bar_x_free), 8);
     for (int i = 0; i < kBwdRowSlots; ++i) mbar_init(smem_u32(&bar_rows_full[i]), 1);
     fence_mbar_init();
   }
@@ -180,11 +193,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     named_bar_sync(1, 128);
-    const int hA = 16 * q + (lane >> 2), hB = hA + 8;
+    // 16x256b fragments of S^T and dP^T (M=64 layout: keys 16q..16q+15 in lanes 0-15 of
+    // quadrant q): this thread holds keys kA = 16q + lane/4 and kB = kA + 8, and heads
+    // 8i + 2(lane&3) + {0,1}, whose D and lse it keeps in registers
+    const int kA = 16 * q + (lane >> 2), kB = kA + 8;
     const int cpair = 2 * (lane & 3);
     const float c2 = p.sm_scale * kLog2e;
-    const float dA = s_delta[hA], dB = s_delta[hB];
-    const float lA = s_lse2[hA], lB = s_lse2[hB];
+    float dh[16], lh[16];
+#pragma unroll
+    for (int i8 = 0; i8 < 8; ++i8)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        dh[2 * i8 + e] = s_delta[8 * i8 + cpair + e];
+        lh[2 * i8 + e] = s_lse2[8 * i8 + cpair + e];
+      }
     for (int b = 0; b < nb && !*abort; ++b) {
       const int rs = b % kBwdRowSlots;
       wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);   // also publishes s_rows[rs]
@@ -206,26 +228,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dv[4 * i8 + e] = __uint_as_float(d4[e]);
       }
+      const bool okA = s_rows[rs][kA] >= 0, okB = s_rows[rs][kB] >= 0;
       tmem_ld_wait();
-      // the previous block's P / dS' tiles have been read by every MMA (dQ^T and dKV^T)
-      if (b >= 1) wait_or_flag(smem_u32(&bar_tiles_free), (b - 1) & 1, abort, lim);
-      const int swA = hA & 7, swB = hB & 7;
+      // P^T and dS'^T as packed bf16 pairs: [i8][0] P key kA, [1] P key kB, [2] dS' kA, [3] dS' kB.
+      // They are formed before the wait for the tiles, which is a wait for dKV^T(b-1) and so for
+      // the drains of block b-1.
+      uint32_t pk[8][4];
 #pragma unroll
       for (int i8 = 0; i8 < 8; ++i8) {
         float pa[2], pb[2], da[2], db[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const bool ok = s_rows[rs][8 * i8 + cpair + e] >= 0;
-          pa[e] = ok ? fast_exp2(fmaf(sv[4 * i8 + e], c2, -lA)) : 0.f;
-          pb[e] = ok ? fast_exp2(fmaf(sv[4 * i8 + 2 + e], c2, -lB)) : 0.f;
-          da[e] = p.sm_scale * pa[e] * (dv[4 * i8 + e] - dA);
-          db[e] = p.sm_scale * pb[e] * (dv[4 * i8 + 2 + e] - dB);
+          pa[e] = okA ? fast_exp2(fmaf(sv[4 * i8 + e], c2, -lh[2 * i8 + e])) : 0.f;
+          pb[e] = okB ? fast_exp2(fmaf(sv[4 * i8 + 2 + e], c2, -lh[2 * i8 + e])) : 0.f;
+          da[e] = p.sm_scale * pa[e] * (dv[4 * i8 + e] - dh[2 * i8 + e]);
+          db[e] = p.sm_scale * pb[e] * (dv[4 * i8 + 2 + e] - dh[2 * i8 + e]);
         }
-        const int off = 2 * cpair;
-        *reinterpret_cast<uint32_t*>(sP + hA * 128 + ((i8 ^ swA) << 4) + off) = pack_bf16x2(pa[0], pa[1]);
-        *reinterpret_cast<uint32_t*>(sP + hB * 128 + ((i8 ^ swB) << 4) + off) = pack_bf16x2(pb[0], pb[1]);
-        *reinterpret_cast<uint32_t*>(sDS + hA * 128 + ((i8 ^ swA) << 4) + off) = pack_bf16x2(da[0], da[1]);
-        *reinterpret_cast<uint32_t*>(sDS + hB * 128 + ((i8 ^ swB) << 4) + off) = pack_bf16x2(db[0], db[1]);
+        pk[i8][0] = pack_bf16x2(pa[0], pa[1]);
+        pk[i8][1] = pack_bf16x2(pb[0], pb[1]);
+        pk[i8][2] = pack_bf16x2(da[0], da[1]);
+        pk[i8][3] = pack_bf16x2(db[0], db[1]);
+      }
+      // the previous block's P / dS' tiles have been read by every MMA (dQ^T and dKV^T)
+      if (b >= 1) wait_or_flag(smem_u32(&bar_tiles_free), (b - 1) & 1, abort, lim);
+      const int swA = kA & 7, swB = kB & 7;
+      const int off = 2 * cpair;
+#pragma unroll
+      for (int i8 = 0; i8 < 8; ++i8) {
+        *reinterpret_cast<uint32_t*>(sP + kA * 128 + ((i8 ^ swA) << 4) + off) = pk[i8][0];
+        *reinterpret_cast<uint32_t*>(sP + kB * 128 + ((i8 ^ swB) << 4) + off) = pk[i8][1];
+        *reinterpret_cast<uint32_t*>(sDS + kA * 128 + ((i8 ^ swA) << 4) + off) = pk[i8][2];
+        *reinterpret_cast<uint32_t*>(sDS + kB * 128 + ((i8 ^ swB) << 4) + off) = pk[i8][3];
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -263,14 +296,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == 0) {
       // ======================================================== issuer A: S, dP, dQ^T
       if (lane == 0 && nb > 0) {
-        constexpr uint32_t id_s = make_idesc_bf16(64, 64, false, false);
-        constexpr uint32_t id_dq = make_idesc_bf16(128, 64, true, false);
-        constexpr uint32_t id_dq64 = make_idesc_bf16(64, 64, true, false);
-        const uint64_t q_k = make_sdesc_sw128(smem_u32(sQ), 16, 1024);      // Q, K-major
-        const uint64_t do_k = make_sdesc_sw128(smem_u32(sDO), 16, 1024);    // dO, K-major
+        constexpr uint32_t id_sd = make_idesc_bf16(64, 128, false, false);  // [S^T | dP^T]
+        constexpr uint32_t id_s = make_idesc_bf16(64, 64, false, false);    // S^T, rope columns
+        constexpr uint32_t id_dq = make_idesc_bf16(128, 64, true, true);
+        constexpr uint32_t id_dq64 = make_idesc_bf16(64, 64, true, true);
+        const uint64_t qd_k = make_sdesc_sw128(smem_u32(sQD), 16, 1024);    // [Q; dO] rows, K-major
         const uint64_t kv_k = make_sdesc_sw128(smem_u32(sKV), 16, 1024);    // K / V rows, K-major
         const uint64_t kv_mn = make_sdesc_sw128(smem_u32(sKV), 8192, 1024); // K^T, MN-major
-        const uint64_t ds_k = make_sdesc_sw128(smem_u32(sDS), 16, 1024);    // dS'^T operand, K-major
+        const uint64_t ds_mn = make_sdesc_sw128(smem_u32(sDS), 8192, 1024); // dS'^T operand, MN-major
         wait_or_flag(smem_u32(&bar_qdo_full), 0, abort, lim);
         for (int b = 0; b < nb && !*abort; ++b) {
           wait_or_flag(smem_u32(&bar_kv_full), b & 1, abort, lim);
@@ -278,17 +311,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           // S and dP: their columns were read by the math warps before p_full(b-1), which this
           // thread waited for before dQ^T(b-1)
+          // [S^T | dP^T] (keys x (64 heads of S, 64 of dP)) = K [Q; dO]^T over the 512 value
+          // columns in one N = 128 chain, then the rope columns add to S^T alone
 #pragma unroll 4
-          for (int ks = 0; ks < kQkSteps; ++ks) {
-            const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-            umma_ss(tmem + kBwdTmemS, q_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
-          }
-#pragma unroll 4
-          for (int ks = 0; ks < 32; ++ks) {
-            const uint32_t off16 = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-            umma_ss(tmem + kBwdTmemDP, do_k + off16, kv_k + off16, id_s, ks > 0 ? 1u : 0u);
-          }
-          umma_commit(smem_u32(&bar_s_full));              // S and dP
+          for (int ks = 0; ks < 32; ++ks)
+            umma_ss(tmem + kBwdTmemS, kv_k + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4),
+                    qd_k + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), id_sd, ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int ks = 32; ks < kQkSteps; ++ks)
+            umma_ss(tmem + kBwdTmemS, kv_k + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4),
+                    qd_k + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), id_s, 1u);
+          umma_commit(smem_u32(&bar_s_full));              // S^T and dP^T
           SMLA_TRACE_EVENT(b, kTrQkIssue);
           wait_or_flag(smem_u32(&bar_p_full), b & 1, abort, lim);
           tc_fence_after();
@@ -297,12 +330,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              umma_ss(tmem + 64 * c, kv_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_dq,
+              umma_ss(tmem + 64 * c, kv_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_dq,
                       (b > 0 || ks > 0) ? 1u : 0u);
           if constexpr (kRope) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              umma_ss(tmem + 256, kv_mn + ((8 * 8192 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_dq64,
+              umma_ss(tmem + 256, kv_mn + ((8 * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_dq64,
                       (b > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(smem_u32(&bar_kv_empty));          // S, dP and dQ^T have read the stage
@@ -317,12 +350,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if (warp == kBwdIssuerB) {
       // ======================================================== issuer B: dKV^T chunks
       if (lane == 0 && nb > 0) {
-        constexpr uint32_t id_kv = make_idesc_bf16(128, 64, true, true);
-        constexpr uint32_t id_kv64 = make_idesc_bf16(64, 64, true, true);
-        const uint64_t q_mn = make_sdesc_sw128(smem_u32(sQ), 8192, 1024);   // Q^T, MN-major
-        const uint64_t do_mn = make_sdesc_sw128(smem_u32(sDO), 8192, 1024); // dO^T, MN-major
-        const uint64_t ds_mn = make_sdesc_sw128(smem_u32(sDS), 8192, 1024); // dS' operand, MN-major
-        const uint64_t p_mn = make_sdesc_sw128(smem_u32(sP), 8192, 1024);   // P operand, MN-major
+        constexpr uint32_t id_kv = make_idesc_bf16(128, 64, true, false);
+        constexpr uint32_t id_kv64 = make_idesc_bf16(64, 64, true, false);
+        const uint64_t q_mn = make_sdesc_sw128(smem_u32(sQD), 16384, 1024);        // Q^T, MN-major
+        const uint64_t do_mn = make_sdesc_sw128(smem_u32(sQD) + 8192, 16384, 1024); // dO^T, MN-major
+        const uint64_t ds_k = make_sdesc_sw128(smem_u32(sDS), 16, 1024);    // dS' operand, K-major
+        const uint64_t p_k = make_sdesc_sw128(smem_u32(sP), 16, 1024);      // P operand, K-major
         uint32_t xu = 0;                              // fills of the dKV^T buffer so far
         wait_or_flag(smem_u32(&bar_qdo_full), 0, abort, lim);
         for (int b = 0; b < nb && !*abort; ++b) {
@@ -337,15 +370,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!kRope || c < 4) {
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
-                umma_ss(col, q_mn + ((2 * c * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv,
+                umma_ss(col, q_mn + ((2 * c * 16384 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_kv,
                         ks > 0 ? 1u : 0u);
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
-                umma_ss(col, do_mn + ((2 * c * 8192 + ks * 2048) >> 4), p_mn + ((ks * 2048) >> 4), id_kv, 1u);
+                umma_ss(col, do_mn + ((2 * c * 16384 + ks * 2048) >> 4), p_k + ((ks * 32) >> 4), id_kv, 1u);
             } else {
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
-                umma_ss(col, q_mn + ((8 * 8192 + ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4), id_kv64,
+                umma_ss(col, q_mn + ((8 * 16384 + ks * 2048) >> 4), ds_k + ((ks * 32) >> 4), id_kv64,
                         ks > 0 ? 1u : 0u);
             }
             umma_commit(smem_u32(&bar_x_full));
@@ -358,13 +391,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         wait_drain(smem_u32(&bar_final_b), 0, lim);
       }
       __syncwarp();
-    } else if (warp >= kBwdDrainWarp0 && warp < kBwdDrainWarp0 + 4) {
+    } else if (warp >= kBwdDrainWarp0 && warp < kBwdDrainWarp0 + 8) {
       // ======================================================== drain (see below)
       // dKV^T chunks of every block, in issue order, into fp32 reductions on the selected rows.
-      // Warp 8+q owns TMEM lanes 32q..32q+31: d = 128c + 32q + lane (or 512 + 16q + lane, lanes
-      // 0-15, for the 64 rope rows), and the 32 lanes of a warp cover 128 contiguous bytes of one
-      // kv row.
-      const int q = warp - kBwdDrainWarp0;
+      // Warps 8+q and 12+q own TMEM lanes 32q..32q+31 (d = 128c + 32q + lane, or 512 + 16q + lane
+      // on lanes 0-15 for the 64 rope rows) and key columns 0-31 and 32-63 of each chunk; the 32
+      // lanes of a warp cover 128 contiguous bytes of one kv row.
+      const int q = warp & 3, hf = (warp - kBwdDrainWarp0) >> 2;   // lane quadrant, key half
       const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
       uint32_t xu = 0;
       for (int b = 0; b < nb && !*abort; ++b) {
@@ -374,72 +407,75 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < kDkvChunks; ++c) {
           wait_or_flag(smem_u32(&bar_x_full), xu & 1, abort, lim);
-          SMLA_TRACE_EVENT_IF(c == 0 && q == 0 && lane == 0, b, kTrSLoaded);
+          SMLA_TRACE_EVENT_IF(c == 0 && q == 0 && hf == 0 && lane == 0, b, kTrSLoaded);
           ++xu;
           tc_fence_after();
           const bool rope = kRope && c == 4;
           const int d = rope ? 512 + 16 * q + lane : 128 * c + 32 * q + lane;
           float* base = p.dkv + d;
           const uint32_t col = kBwdTmemX;
-          // two halves of 32 keys; the buffer goes back once both are in registers
+          // this warp's 32 keys; the buffer goes back once every drain warp has its half
+          uint32_t v[32];
+          tmem_ld16(tmem + lane_base + col + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+          tmem_ld16(tmem + lane_base + col + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_x_free));
+          if (!rope || lane < 16) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t v[32];
-            tmem_ld16(tmem + lane_base + col + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-            tmem_ld16(tmem + lane_base + col + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-            tmem_ld_wait();
-            if (half == 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(&bar_x_free));
-            }
-            if (!rope || lane < 16) {
-#pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                const int row = s_rows[rs][32 * half + k];
-                if (row >= 0) atomicAdd(base + static_cast<int64_t>(row) * D_QK, __uint_as_float(v[k]));
-              }
+            for (int k = 0; k < 32; ++k) {
+              const int row = s_rows[rs][32 * hf + k];
+              if (row >= 0) atomicAdd(base + static_cast<int64_t>(row) * D_QK, __uint_as_float(v[k]));
             }
           }
         }
       }
-      SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, nb, kTrSent);
+      SMLA_TRACE_EVENT_IF(q == 0 && hf == 0 && lane == 0, nb, kTrSent);
     } else {
       // ======================================================== gather (see below)
-      // warps 1-3 and 13-15; the first loads the item's Q and dO tiles and publishes each block's
+      // warps 1-2 and 16-23; the first loads the item's Q and dO tiles and publishes each block's
       // row table (TMA row coordinates, -1 for slots that do not count)
-      const int gw = warp < 4 ? warp - 1 : warp - 10;   // 0..5
+      const int gw = warp < 3 ? warp - 1 : warp - 14;   // 0..9
       const bool leader = (gw == 0 && lane == 0);
       if (leader && nb > 0) {
         mbar_arrive_expect_tx(smem_u32(&bar_qdo_full), (kChunks + 8) * 8192u);
         for (int c = 0; c < kChunks; ++c)
-          tma_load_2d(smem_u32(sQ + c * 8192), &q_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
+          tma_load_2d(smem_u32(sQD + c * 16384), &q_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
         for (int c = 0; c < 8; ++c)
-          tma_load_2d(smem_u32(sDO + c * 8192), &do_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
+          tma_load_2d(smem_u32(sQD + c * 16384 + 8192), &do_map, 64 * c, static_cast<int>(qrow), smem_u32(&bar_qdo_full));
       }
-      const int it = gw + kBwdGatherWarps * lane;       // (4-row group, chunk) item of a block
-      const int grp = it & 15, chunk = it >> 4;
-      const bool issues = it < 16 * kChunks;
+      // (4-row group, chunk) items of a block: item gw + 2 (lane + 32 j) for j < kGI
+      constexpr int kGI = (16 * kChunks + 32 * kBwdGatherWarps - 1) / (32 * kBwdGatherWarps);
+      auto item_of = [&](int j) { return gw + kBwdGatherWarps * (lane + 32 * j); };
       // the rows of block b+1 are loaded while block b is in flight (indices come from HBM)
-      auto rows4 = [&](int b) {
-        const int j = 64 * b + 4 * grp;
-        return make_int4(bwd_row(p, idx_row, j, L), bwd_row(p, idx_row, j + 1, L), bwd_row(p, idx_row, j + 2, L),
-                         bwd_row(p, idx_row, j + 3, L));
+      auto rows4 = [&](int b, int j) {
+        const int r0 = 64 * b + 4 * (item_of(j) & 15);
+        return make_int4(bwd_row(p, idx_row, r0, L), bwd_row(p, idx_row, r0 + 1, L), bwd_row(p, idx_row, r0 + 2, L),
+                         bwd_row(p, idx_row, r0 + 3, L));
       };
       auto rows2 = [&](int b) {
         return make_int2(bwd_row(p, idx_row, 64 * b + lane, L), bwd_row(p, idx_row, 64 * b + lane + 32, L));
       };
-      int4 nxt4 = make_int4(-1, -1, -1, -1);
+      int4 nxt4[kGI];
       int2 nxt2 = make_int2(-1, -1);
+#pragma unroll
+      for (int j = 0; j < kGI; ++j) nxt4[j] = make_int4(-1, -1, -1, -1);
       if (nb > 0) {
-        if (issues) nxt4 = rows4(0);
+#pragma unroll
+        for (int j = 0; j < kGI; ++j)
+          if (item_of(j) < 16 * kChunks) nxt4[j] = rows4(0, j);
         if (gw == 0) nxt2 = rows2(0);
       }
       for (int b = 0; b < nb && !*abort; ++b) {
-        const int4 cur4 = nxt4;
+        int4 cur4[kGI];
+#pragma unroll
+        for (int j = 0; j < kGI; ++j) cur4[j] = nxt4[j];
         const int2 cur2 = nxt2;
         if (b + 1 < nb) {
-          if (issues) nxt4 = rows4(b + 1);
+#pragma unroll
+          for (int j = 0; j < kGI; ++j)
+            if (item_of(j) < 16 * kChunks) nxt4[j] = rows4(b + 1, j);
           if (gw == 0) nxt2 = rows2(b + 1);
         }
         if (b >= 1) wait_or_flag(smem_u32(&bar_kv_empty), (b - 1) & 1, abort, lim);
@@ -458,9 +494,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive_expect_tx(smem_u32(&bar_kv_full), kChunks * 8192u);
           }
         }
-        if (issues)
-          tma_gather4(smem_u32(sKV + chunk * 8192 + grp * 512), &kv_map, 64 * chunk, cur4.x, cur4.y, cur4.z, cur4.w,
-                      smem_u32(&bar_kv_full));
+#pragma unroll
+        for (int j = 0; j < kGI; ++j) {
+          const int it = item_of(j), chunk = it >> 4;
+          if (it < 16 * kChunks)
+            tma_gather4(smem_u32(sKV + chunk * 8192 + (it & 15) * 512), &kv_map, 64 * chunk, cur4[j].x, cur4[j].y,
+                        cur4[j].z, cur4[j].w, smem_u32(&bar_kv_full));
+        }
       }
       // the Q / dO tiles and the last block have landed before this CTA may exit
       if (leader && nb > 0) {
