@@ -77,6 +77,18 @@ struct BwdParams {
   uint64_t wait_limit_ns;
 };
 
+// tcgen05.ld 16x32bx2, 16 columns per half, halves 16 columns apart: threads 0-15 read lanes
+// base + t at columns col .. col+15, threads 16-31 read lanes base + t - 16 at col+16 .. col+31
+__device__ __forceinline__ void tmem_ld_16x32bx2_x16_off16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 16;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 // TMA row coordinate of slot j of row t (j < L): the kv row, or -1 when the slot does not count
 __device__ __forceinline__ int bwd_row(const BwdParams& p, const int32_t* idx_row, int j, int L) {
   if (j >= L) return -1;
@@ -396,7 +408,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // dKV^T chunks of every block, in issue order, into fp32 reductions on the selected rows.
       // Warps 8+q and 12+q own TMEM lanes 32q..32q+31 (d = 128c + 32q + lane, or 512 + 16q + lane
       // on lanes 0-15 for the 64 rope rows) and key columns 0-31 and 32-63 of each chunk; the 32
-      // lanes of a warp cover 128 contiguous bytes of one kv row.
+      // lanes of a warp cover 128 contiguous bytes of one kv row.  The reductions are bound by
+      // their instruction count, so every one of them carries 32 values: on the rope chunk the
+      // two thread halves take different keys.
       const int q = warp & 3, hf = (warp - kBwdDrainWarp0) >> 2;   // lane quadrant, key half
       const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
       uint32_t xu = 0;
@@ -410,19 +424,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           SMLA_TRACE_EVENT_IF(c == 0 && q == 0 && hf == 0 && lane == 0, b, kTrSLoaded);
           ++xu;
           tc_fence_after();
-          const bool rope = kRope && c == 4;
-          const int d = rope ? 512 + 16 * q + lane : 128 * c + 32 * q + lane;
-          float* base = p.dkv + d;
           const uint32_t col = kBwdTmemX;
-          // this warp's 32 keys; the buffer goes back once every drain warp has its half
-          uint32_t v[32];
-          tmem_ld16(tmem + lane_base + col + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-          tmem_ld16(tmem + lane_base + col + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bar_x_free));
-          if (!rope || lane < 16) {
+          if (kRope && c == 4) {
+            // the 64 rope rows sit on lanes 0-15 of each quadrant: both thread halves take part,
+            // threads 16-31 on the second 16 of this warp's 32 keys, so 16 reductions cover them
+            uint32_t v[16];
+            tmem_ld_16x32bx2_x16_off16(tmem + lane_base + col + 32 * hf, v);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_x_free));
+            float* base = p.dkv + 512 + 16 * q + (lane & 15);
+            const int k0 = 32 * hf + 16 * (lane >> 4);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int row = s_rows[rs][k0 + k];
+              if (row >= 0) atomicAdd(base + static_cast<int64_t>(row) * D_QK, __uint_as_float(v[k]));
+            }
+          } else {
+            float* base = p.dkv + 128 * c + 32 * q + lane;
+            // this warp's 32 keys; the buffer goes back once every drain warp has its half
+            uint32_t v[32];
+            tmem_ld16(tmem + lane_base + col + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+            tmem_ld16(tmem + lane_base + col + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_x_free));
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int row = s_rows[rs][32 * hf + k];
