@@ -56,7 +56,7 @@ def _bind(lib):
     lib.smla_oracle_fwd.argtypes = [P, P, P, P, P, D, I64, I64, I32, I32, I32, I32, P, I64,
                                     P, P, P, I32]
     lib.smla_oracle_fwd_paged.restype = ctypes.c_int
-    lib.smla_oracle_fwd_paged.argtypes = [P, P, P, P, I64, I32, I32, I32, P, P, P, D, I64,
+    lib.smla_oracle_fwd_paged.argtypes = [P, P, I64, P, P, I64, I32, I32, I32, P, P, P, D, I64,
                                           I32, I32, I32, I32, P, I64, P, P, P, I32]
     lib.smla_oracle_last_valid_length.restype = None
     lib.smla_oracle_last_valid_length.argtypes = [P, I64, I32, I64, P]
@@ -112,7 +112,10 @@ def sparse_mla_fwd(q_bits, kv_bits, indices, topk_length=None, attn_sink=None, s
 def sparse_mla_fwd_paged(q_bits, kv_pool_bits, block_table, indices, page_block=64,
                          seqlens_k=None, s_kv_per_req=0, s_q_per_req=1, topk_length=None,
                          attn_sink=None, sm_scale=None, d_v=512, rows=None, threads=0, _lib_=None):
-    """fp64 reference over a paged KV cache; same outputs as :func:`sparse_mla_fwd`."""
+    """fp64 reference over a paged KV cache [pool_rows, 1, d_qk] with a block table
+    [n_req, max_blocks]; same outputs as :func:`sparse_mla_fwd`.  A position past the request's
+    length or its table row, on a negative table entry, or on a row past the pool is an invalid
+    slot."""
     lib = _lib_ or _load()
     q_bits = _c(q_bits, np.uint16)
     kv_pool_bits = _c(kv_pool_bits, np.uint16)
@@ -131,7 +134,8 @@ def sparse_mla_fwd_paged(q_bits, kv_pool_bits, block_table, indices, page_block=
     sk = _c(seqlens_k, np.int32)
     tl = _c(topk_length, np.int32)
     sink = _c(attn_sink, np.float32)
-    rc = lib.smla_oracle_fwd_paged(_ptr(q_bits), _ptr(kv_pool_bits), _ptr(block_table), _ptr(sk),
+    pool_rows = kv_pool_bits.shape[0]
+    rc = lib.smla_oracle_fwd_paged(_ptr(q_bits), _ptr(kv_pool_bits), pool_rows, _ptr(block_table), _ptr(sk),
                                    int(s_kv_per_req), max_blocks, int(page_block), int(s_q_per_req),
                                    _ptr(indices), _ptr(tl), _ptr(sink), float(sm_scale), s_q, h_q,
                                    d_qk, d_v, topk, _ptr(rows_arr), n, _ptr(out), _ptr(lse),

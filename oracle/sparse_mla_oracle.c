@@ -122,20 +122,30 @@ static const uint16_t* flat_resolve(const void* vctx, int64_t t, int32_t idx) {
 
 /* ------------------------------------------------------------------ paged KV cache */
 typedef struct {
-  const uint16_t* kv_pool;      /* [n_pages * page_block, d_qk] */
+  const uint16_t* kv_pool;      /* [pool_rows, d_qk] */
   const int32_t* block_table;   /* [n_req, max_blocks] */
   const int32_t* seqlens_k;     /* [n_req] or NULL */
-  int64_t s_kv_per_req;
+  int64_t s_kv_per_req, pool_rows;
   int max_blocks, page_block, s_q_per_req, d_qk;
 } paged_ctx;
 
+/* Token position idx of the request that query row t belongs to, resolved to its pool row
+ * (FlashMLA PR #216, "Summary": indices are token positions of the request, and a position
+ * that is not valid is never used as an address).  Reading of the paged layout: a position
+ * counts only if it lies in the request (0 <= idx < its length), its page lies inside the
+ * request's block-table row, the table entry is a page (not negative), and the resulting row
+ * lies inside the pool.  Anything else is an invalid slot, like -1 in the flat form. */
 static const uint16_t* paged_resolve(const void* vctx, int64_t t, int32_t idx) {
   const paged_ctx* c = (const paged_ctx*)vctx;
   int64_t b = t / c->s_q_per_req;
   int64_t len = c->seqlens_k ? (int64_t)c->seqlens_k[b] : c->s_kv_per_req;
   if (idx < 0 || (int64_t)idx >= len) return NULL; /* token position must lie in the request */
-  int64_t page = c->block_table[b * c->max_blocks + idx / c->page_block];
+  int64_t blk = idx / c->page_block;
+  if (blk >= c->max_blocks) return NULL;           /* page beyond the request's table row */
+  int64_t page = c->block_table[b * c->max_blocks + blk];
+  if (page < 0) return NULL;                       /* unmapped page */
   int64_t row = page * c->page_block + idx % c->page_block;
+  if (row >= c->pool_rows) return NULL;            /* row off the end of the pool */
   return c->kv_pool + row * c->d_qk;
 }
 
@@ -197,21 +207,23 @@ int smla_oracle_fwd(const uint16_t* q, const uint16_t* kv, const int32_t* indice
                   n_rows, out, lse, max_logits, n_threads, flat_resolve, &ctx);
 }
 
-/* Same forward over a paged KV cache (FlashMLA PR #216, "Dynamic top-k": indices are token
+/* Same forward over a paged KV cache (FlashMLA PR #216, "Summary": indices are token
  * positions of the request; the cache is stored in pages of `page_block` tokens).  Query row
  * t belongs to request t / s_q_per_req; token position p of request b lives in pool row
- * block_table[b][p / page_block] * page_block + p % page_block.  Position p is valid iff
- * 0 <= p < seqlens_k[b] (or s_kv_per_req when seqlens_k is NULL). */
-int smla_oracle_fwd_paged(const uint16_t* q, const uint16_t* kv_pool, const int32_t* block_table,
+ * block_table[b][p / page_block] * page_block + p % page_block of the pool's pool_rows rows.
+ * Position p is valid iff 0 <= p < seqlens_k[b] (or s_kv_per_req when seqlens_k is NULL),
+ * p / page_block < max_blocks, the table entry is >= 0 and the row is < pool_rows. */
+int smla_oracle_fwd_paged(const uint16_t* q, const uint16_t* kv_pool, int64_t pool_rows,
+                          const int32_t* block_table,
                           const int32_t* seqlens_k, int64_t s_kv_per_req, int max_blocks,
                           int page_block, int s_q_per_req, const int32_t* indices,
                           const int32_t* topk_length, const float* attn_sink, double sm_scale,
                           int64_t s_q, int h_q, int d_qk, int d_v, int topk, const int64_t* rows,
                           int64_t n_rows, double* out, double* lse, double* max_logits,
                           int n_threads) {
-  if (page_block <= 0 || s_q_per_req <= 0 || max_blocks <= 0) return -1;
-  paged_ctx ctx = {kv_pool, block_table, seqlens_k, s_kv_per_req, max_blocks, page_block,
-                   s_q_per_req, d_qk};
+  if (page_block <= 0 || s_q_per_req <= 0 || max_blocks <= 0 || pool_rows < 0) return -1;
+  paged_ctx ctx = {kv_pool, block_table, seqlens_k, s_kv_per_req, pool_rows, max_blocks,
+                   page_block, s_q_per_req, d_qk};
   return run_rows(q, indices, topk_length, attn_sink, sm_scale, s_q, h_q, d_qk, d_v, topk, rows,
                   n_rows, out, lse, max_logits, n_threads, paged_resolve, &ctx);
 }

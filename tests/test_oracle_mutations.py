@@ -38,9 +38,14 @@ MUTATIONS = [
     ("paged offset within a page", "int64_t row = page * c->page_block + idx % c->page_block;",
      "int64_t row = page * c->page_block + (idx + 1) % c->page_block;"),
     ("paged block table ignored",
-     "int64_t page = c->block_table[b * c->max_blocks + idx / c->page_block];",
-     "int64_t page = b * c->max_blocks + idx / c->page_block;"),
+     "int64_t page = c->block_table[b * c->max_blocks + blk];",
+     "int64_t page = b * c->max_blocks + blk;"),
     ("tail length off by one", "L = j + 1;", "L = j;"),
+    ("paged table bound clamped instead of masked",
+     "if (blk >= c->max_blocks) return NULL;", "if (blk >= c->max_blocks) blk = c->max_blocks - 1;"),
+    ("unmapped page read as page 0", "if (page < 0) return NULL;", "if (page < 0) page = 0;"),
+    ("off-pool row clamped instead of masked",
+     "if (row >= c->pool_rows) return NULL;", "if (row >= c->pool_rows) row = c->pool_rows - 1;"),
 ]
 
 

@@ -10,7 +10,9 @@ Each test below checks the oracle against something the pages or plain mathemati
   * closed forms (uniform logits, one slot, two slots, duplicated slot, value-less sink key:
     FlashMLA PR #198 "Summary" item 2) including the hand-derived fixtures in
     tests/golden/closed_forms.json;
-  * the paged address translation against an explicit per-request gather.
+  * the paged address translation against an explicit per-request gather, and the paged
+    validity rule (positions past the table row, unmapped pages, rows past the pool) against
+    an independent numpy resolution into flat pool rows.
 A plausible mistake in the oracle (dropped scale, wrong index, transposed operand, wrong V
 columns, lse in the wrong base or including the sink, wrong validity bound, wrong clamp)
 fails at least one of them.
@@ -301,6 +303,66 @@ def test_paged_equals_explicit_per_request_gather(orc):
         np.testing.assert_array_equal(O[b], Ob[0])
         np.testing.assert_array_equal(lse[b], lseb[0])
         np.testing.assert_array_equal(mx[b], mxb[0])
+
+
+def _paged_to_flat_rows(bt, idx, page, lengths, pool_rows, s_q_per_req=1):
+    """Paged reading restated in numpy: each slot's token position becomes its pool row, or -1
+    when the position is outside the request, past the request's block-table row, on a
+    negative (unmapped) table entry, or on a row past the end of the pool."""
+    s_q, topk = idx.shape[0], idx.shape[-1]
+    max_blocks = bt.shape[1]
+    flat = np.full((s_q, 1, topk), -1, np.int32)
+    for t in range(s_q):
+        b = t // s_q_per_req
+        for j in range(topk):
+            p = int(idx[t, 0, j])
+            if p < 0 or p >= lengths[b] or p // page >= max_blocks:
+                continue
+            pg = int(bt[b, p // page])
+            row = pg * page + p % page
+            if pg < 0 or row >= pool_rows:
+                continue
+            flat[t, 0, j] = row
+    return flat
+
+
+def test_paged_positions_off_the_table_or_pool_are_invalid(orc):
+    # Positions whose page lies past the request's block-table row, table entries that are
+    # negative, and pages that run off the end of the pool are invalid slots (FlashMLA PR #216,
+    # "Summary": a position that is not valid is never used as an address).  The paged oracle
+    # must equal the flat oracle over the whole pool, with each slot resolved independently.
+    rng = np.random.default_rng(23)
+    n_req, s_q_per_req, page, max_blocks, h, d, topk = 4, 2, 8, 3, 2, 16, 30
+    s_kv_per_req = 40                       # longer than the 24 positions the table covers
+    n_pages = 16
+    pool_rows = n_pages * page - 5          # the last page is partly off the pool
+    pool = bits(rng.standard_normal((pool_rows, 1, d)))
+    bt = rng.choice(n_pages - 1, size=(n_req, max_blocks), replace=False).astype(np.int32)
+    bt[0, 1] = -1                           # unmapped page
+    bt[1, 2] = n_pages - 1                  # page partly past the pool
+    bt[2, 0] = n_pages + 3                  # page wholly past the pool
+    bt[3, 2] = -7
+    s_q = n_req * s_q_per_req
+    q = bits(rng.standard_normal((s_q, h, d)))
+    idx = rng.integers(-2, s_kv_per_req + 4, size=(s_q, 1, topk)).astype(np.int32)
+    idx[0, 0, :4] = [8, 9, 15, 30]          # on the unmapped page, and past the table
+    idx[2, 0, :3] = [16 + 2, 16 + 7, 21]    # on the partly-off page: row 122 valid, 127 and 125 not
+    idx[4, 0, :3] = [0, 5, 7]               # on the page wholly past the pool
+    sink = rng.standard_normal(h).astype(np.float32)
+    lengths = np.full(n_req, s_kv_per_req)
+    flat_idx = _paged_to_flat_rows(bt, idx, page, lengths, pool_rows, s_q_per_req)
+    assert (flat_idx >= 0).sum() > 20 and (flat_idx < 0).sum() > 20
+    got = orc.sparse_mla_fwd_paged(q, pool, bt, idx, page_block=page, s_kv_per_req=s_kv_per_req,
+                                   s_q_per_req=s_q_per_req, attn_sink=sink, d_v=12)
+    ref = orc.sparse_mla_fwd(q, pool, flat_idx, attn_sink=sink, d_v=12)
+    for x, y in zip(got, ref):
+        np.testing.assert_array_equal(x, y)
+    # a row whose every position is invalid in these ways is an exactly empty row
+    idx2 = idx.copy()
+    idx2[1, 0, :] = 8                       # request 0, unmapped page only
+    got2 = orc.sparse_mla_fwd_paged(q, pool, bt, idx2, page_block=page, s_kv_per_req=s_kv_per_req,
+                                    s_q_per_req=s_q_per_req, attn_sink=sink, d_v=12)
+    assert np.all(got2[0][1] == 0) and np.all(got2[1][1] == np.inf) and np.all(got2[2][1] == -np.inf)
 
 
 def test_last_valid_length_matches_definition_and_is_neutral(orc):

@@ -280,6 +280,41 @@ def test_paged_per_request_lengths(with_len):
     assert_parity(to_np(run_gpu(w)), run_oracle(w), f"paged seqlens len={with_len}")
 
 
+def _paged_edge_case(seed, n_req=5, s_q_per_req=2, page=64, max_blocks=6, h_q=64, d_qk=576, topk=520):
+    """Paged cache whose requests are longer than their block-table rows (positions past the
+    table), with unmapped (negative) table entries and pages that run off the end of the pool."""
+    rng = np.random.default_rng(seed)
+    n_pages = n_req * max_blocks + 4
+    pool_rows = n_pages * page - 21              # the last page is partly off the pool
+    pool = W.normal_bf16(rng, (pool_rows, 1, d_qk))
+    bt = rng.permutation(n_pages - 1)[: n_req * max_blocks].astype(np.int32).reshape(n_req, max_blocks)
+    bt[0, 1] = -1
+    bt[1, 3] = n_pages - 1                       # partly past the pool
+    bt[2, 0] = n_pages + 5                       # wholly past the pool
+    bt[3, 5] = -100
+    s_kv_per_req = max_blocks * page + 150       # positions up to 150 past each table row
+    s_q = n_req * s_q_per_req
+    q = W.normal_bf16(rng, (s_q, h_q, d_qk))
+    idx = rng.integers(-2, s_kv_per_req + 8, size=(s_q, 1, topk)).astype(np.int32)
+    idx[2, 0, :64] = 3 * page + np.arange(64)    # request 1, the partly-off page
+    idx[0, 0, :] = page + rng.integers(0, page, size=topk)   # request 0, unmapped page only
+    return dict(q=q, kv=pool, indices=idx, topk_length=None,
+                attn_sink=rng.standard_normal(h_q).astype(np.float32),
+                sm_scale=float(np.float32(1 / np.sqrt(d_qk))), d_v=512, paged=True, block_table=bt,
+                page_block=page, s_kv_per_req=s_kv_per_req, s_q_per_req=s_q_per_req, seqlens_k=None)
+
+
+@pytest.mark.parametrize("n_split", [1, 3])
+def test_paged_positions_off_the_table_or_pool(n_split):
+    # positions whose page lies past the request's table row, negative table entries and rows
+    # past the pool are invalid slots on both sides; row 0 has only such slots and is empty
+    w = _paged_edge_case(41)
+    gpu = to_np(run_gpu(w, n_split=n_split))
+    ref = run_oracle(w)
+    assert np.all(ref[1][0] == np.inf)
+    assert_parity(gpu, ref, f"paged edge positions n_split={n_split}")
+
+
 # ---------------------------------------------------------------- split-KV
 @pytest.mark.parametrize("case", CASES, ids=[f"s{c[0]}" for c in CASES])
 @pytest.mark.parametrize("n_split", [2, 5, 64])
