@@ -198,7 +198,9 @@ smla_status sparse_mla_selftest_wait_timeout(uint64_t limit_ns, smla_stream_t st
  *                                          then accumulated; zeroed otherwise)
  * Every row's work is bounded by L_t (topk_length, or topk); slots in [0, L_t) that do not
  * count are masked.  Uses no workspace and allocates nothing.  With s_q == 0, dkv and dsink
- * are zeroed and nothing else happens.
+ * are zeroed and nothing else happens.  Every error except SMLA_ERR_LAUNCH is returned before
+ * anything is enqueued; SMLA_ERR_LAUNCH may come after the zeroing of dkv and dsink was
+ * queued, which then leaves them zeroed.
  */
 smla_status sparse_mla_bwd(const void* q, const void* kv, const void* out, const void* dout,
                            const int32_t* indices, const int32_t* topk_length, const float* attn_sink,

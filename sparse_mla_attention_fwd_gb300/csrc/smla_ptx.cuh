@@ -1,5 +1,6 @@
-// Thin inline-PTX layer for sm_103a: mbarriers, cp.async, tcgen05 (TMEM alloc, UMMA issue,
-// commit, TMEM load/store) and the two descriptor encodings UMMA needs.
+// Thin inline-PTX layer for sm_103a: mbarriers, TMA (2-D tiles and gather4), tcgen05 (TMEM
+// alloc, UMMA issue, commit, TMEM load/store), ldmatrix, setmaxnreg, and the two descriptor
+// encodings UMMA needs.
 //
 // Everything here is a one-instruction wrapper; the kernel decides the protocol.  Encodings
 // follow the PTX ISA description of the tcgen05 instruction descriptor (kind::f16) and the
@@ -22,16 +23,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "elect.sync _|P, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, P;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -86,28 +77,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
-// ---------------------------------------------------------------- proxies / cp.async
+// ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// 16-byte global->shared copy; bytes beyond `src_bytes` (0 or 16) are zero-filled, and with
-// src_bytes == 0 the source is not read at all.
-__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Arrive on `bar` when all prior cp.async of this thread have landed (no pending-count increment).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05: TMEM management
@@ -272,23 +244,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int x
 
 namespace smla {
 
-// Non-blocking probe of an mbarrier phase (never suspends the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, P;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-}  // namespace smla
-
-namespace smla {
-
 // Per-warpgroup register rebalancing (every warp of a warpgroup executes the same one).
 template <int N>
 __device__ __forceinline__ void reg_alloc() {
@@ -303,68 +258,6 @@ __device__ __forceinline__ void reg_dealloc() {
 
 namespace smla {
 
-// ---------------------------------------------------------------- clusters / DSMEM
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Address of the same shared-memory location in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
-// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior writes
-// at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// try_wait with cluster-scope acquire (for barriers that receive remote arrivals).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, P;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
-                                                          volatile int* abort, uint64_t limit_ns) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((++spins & 63u) == 0u) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init_cluster() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
 // 16 lanes x 256 bits: thread t of the warp gets rows (t>>2) and (t>>2)+8 of the 16-lane
 // group that starts at the address' lane, columns 2(t&3) and 2(t&3)+1 of the 8 columns that
 // start at the address' column: r[0..1] = row (t>>2), r[2..3] = row (t>>2)+8.
@@ -372,14 +265,6 @@ __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]
   asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(taddr));
-}
-
-// Store counterpart of tmem_ld_16x256b (same thread -> lane / column mapping).
-__device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, uint32_t r0, uint32_t r1,
-                                                uint32_t r2, uint32_t r3) {
-  asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
-               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-               : "memory");
 }
 
 // 16 lanes x 128 bits, 8 repetitions along the columns (32 columns): thread t stores r[2i] to
@@ -402,32 +287,6 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t& r0, uint
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(saddr)
-               : "memory");
-}
-
-}  // namespace smla
-
-namespace smla {
-
-// Asynchronous 16-byte store into another CTA's shared memory; its bytes complete on the
-// mbarrier `cluster_bar` of that CTA (which must expect them as transaction bytes).
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          cluster_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
-      : "memory");
-}
-
-}  // namespace smla
-
-namespace smla {
-
-// Remote arrive without release semantics: for "buffer consumed" signals whose reads have
-// already completed (their values were used), so no fence is needed.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 

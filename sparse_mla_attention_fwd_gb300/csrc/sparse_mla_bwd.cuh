@@ -547,15 +547,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 template <int D_QK>
+constexpr size_t bwd_smem_bytes() {
+  return (2 * (D_QK / 64) + 10) * 8192 + 1024;
+}
+
+// Sets the kernel's shared-memory attribute (before anything is enqueued).
+template <int D_QK>
+smla_status prepare_bwd() {
+  return cudaFuncSetAttribute(sparse_mla_bwd_kernel<D_QK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(bwd_smem_bytes<D_QK>())) == cudaSuccess
+             ? SMLA_OK
+             : SMLA_ERR_LAUNCH;
+}
+
+template <int D_QK>
 smla_status launch_bwd(const CUtensorMap& qm, const CUtensorMap& dom, const CUtensorMap& kvm, const BwdParams& p,
                        int64_t n_items, cudaStream_t stream) {
-  auto kern = sparse_mla_bwd_kernel<D_QK>;
-  constexpr int kChunks = D_QK / 64;
-  const size_t smem = (2 * kChunks + 10) * 8192 + 1024;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return SMLA_ERR_LAUNCH;
-  kern<<<static_cast<unsigned>(n_items), kBwdThreads, smem, stream>>>(qm, dom, kvm, p);
+  sparse_mla_bwd_kernel<D_QK><<<static_cast<unsigned>(n_items), kBwdThreads, bwd_smem_bytes<D_QK>(), stream>>>(
+      qm, dom, kvm, p);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
 }
 
@@ -575,17 +584,23 @@ smla_status bwd_flat(const void* q, const void* kv, const void* out, const void*
   }
   if (s_kv > 0 && !dkv) return SMLA_ERR_NULL_PTR;
   if ((dkv && !aligned4(dkv)) || (dsink && !aligned4(dsink))) return SMLA_ERR_MISALIGNED;
+  // tensor maps and the kernel attribute come before the memsets, so that every error but a
+  // failed launch itself is returned before anything is enqueued
+  CUtensorMap qm, dom, kvm;
+  if (s_q > 0) {
+    const uint64_t rows = static_cast<uint64_t>(s_q) * h_q;
+    if (!make_map(&qm, q, rows, d_qk, 64) || !make_map(&dom, dout, rows, d_v, 64)) return SMLA_ERR_TENSOR_MAP;
+    if (!make_map(&kvm, s_kv > 0 ? kv : q, s_kv > 0 ? static_cast<uint64_t>(s_kv) : 1u, d_qk, 1))
+      return SMLA_ERR_TENSOR_MAP;
+    st = d_qk == 512 ? prepare_bwd<512>() : prepare_bwd<576>();
+    if (st != SMLA_OK) return st;
+  }
   // dkv and dsink are accumulated into: they start at zero
   if (s_kv > 0 && cudaMemsetAsync(dkv, 0, static_cast<size_t>(s_kv) * d_qk * sizeof(float), stream) != cudaSuccess)
     return SMLA_ERR_LAUNCH;
   if (dsink && cudaMemsetAsync(dsink, 0, static_cast<size_t>(h_q) * sizeof(float), stream) != cudaSuccess)
     return SMLA_ERR_LAUNCH;
   if (s_q == 0) return SMLA_OK;
-  CUtensorMap qm, dom, kvm;
-  const uint64_t rows = static_cast<uint64_t>(s_q) * h_q;
-  if (!make_map(&qm, q, rows, d_qk, 64) || !make_map(&dom, dout, rows, d_v, 64)) return SMLA_ERR_TENSOR_MAP;
-  if (!make_map(&kvm, s_kv > 0 ? kv : q, s_kv > 0 ? static_cast<uint64_t>(s_kv) : 1u, d_qk, 1))
-    return SMLA_ERR_TENSOR_MAP;
   BwdParams p{};
   p.indices = indices;
   p.topk_length = topk_length;

@@ -92,8 +92,9 @@ enum : uint32_t { kFirstBlock = 1u, kLastBlock = 2u };
 __device__ int g_device_status = 0;    // SMLA_ERR_DEVICE_TIMEOUT once any wait gave up
 
 // Scratch of the allocation-free split-KV entry point (sparse_mla_fwd_paged_splitkv_static):
-// 32 MiB, enough for e.g. 8 rows x 2 head groups x 16 ranges.  Every unit writes its whole
-// partial result before the merge reads it, so no part of it has to start at zero.
+// 32 MiB.  Each (row, head group, range) unit takes 131840 bytes of partial O and statistics,
+// so up to 254 units fit, e.g. 8 rows x 2 head groups x 15 ranges.  Every unit writes its
+// whole partial result before the merge reads it, so no part of it has to start at zero.
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) uint8_t g_splitkv_scratch[kStaticScratchBytes];
 
@@ -1127,7 +1128,8 @@ smla_status set_split(FwdParams& p, int64_t s_q, int h_q, int n_split, void* wor
   if (n_split < 1 || n_split > kMaxSplit) return SMLA_ERR_BAD_SHAPE;
   if (s_q * (h_q / kGroupHeads) * static_cast<int64_t>(n_split) > INT32_MAX) return SMLA_ERR_BAD_SHAPE;
   p.n_split = n_split;
-  if (n_split == 1) return SMLA_OK;
+  // one range needs no workspace; with no rows nothing runs and no pointer is inspected
+  if (n_split == 1 || s_q == 0) return SMLA_OK;
   if (!workspace) return SMLA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SMLA_ERR_MISALIGNED;
   size_t stats_off = 0;

@@ -115,6 +115,7 @@ def test_splitkv_workspace_size_and_argument_checks(lib):
     assert call(nbytes=1000) == 7                   # too small
     assert call(ws=FAKE + 16) == 3                  # not 256-byte aligned
     assert call(s_q=0, q=None, kv=None, idx=None, out=None) == 0
+    assert call(s_q=0, ws=None) == 0                # no rows: the workspace is not inspected
 
 
 def call_bwd(lib, q=FAKE, kv=FAKE, out=FAKE, dout=FAKE, idx=FAKE, tl=None, sink=None, lse=FAKE, scale=0.04,

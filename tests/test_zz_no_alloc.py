@@ -55,6 +55,12 @@ def test_oversized_problems_are_rejected_before_launch():
         fake, fake, 4096, fake, 64, 64, None, 4096, 1, fake, None, None, ctypes.c_float(0.04), 512,
         fake, fake, fake, 2, 128, 576, 2048, 64, None)
     assert rc == 7   # SMLA_ERR_WORKSPACE
+    # no rows: a no-op that returns SMLA_OK whatever n_split is (no scratch lookup, no launch)
+    for n_split in (1, 2, 64):
+        rc = lib.sparse_mla_fwd_paged_splitkv_static(
+            fake, fake, 4096, fake, 64, 64, None, 4096, 1, fake, None, None, ctypes.c_float(0.04), 512,
+            fake, fake, fake, 0, 128, 576, 2048, n_split, None)
+        assert rc == 0, (n_split, rc)
 
 
 @pytest.mark.gpu
