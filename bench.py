@@ -24,7 +24,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import subprocess
 import sys
 import time
@@ -59,8 +58,10 @@ def parse():
                     help="split-KV ranges per row: 'auto' (split only when items < SMs) or an integer")
     ap.add_argument("--with-len", action="store_true", help="pass topk_length in the timed steps")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-chunks", type=int, default=8, help="row chunks of the host-buffer end-to-end leg")
     ap.add_argument("--skip-cpu", action="store_true", help="no CPU-oracle baseline leg")
     ap.add_argument("--skip-e2e", action="store_true", help="no host-buffer end-to-end leg")
+    ap.add_argument("--skip-decode", action="store_true", help="no decode fixed-vs-dynamic leg")
     ap.add_argument("--no-clocks", action="store_true")
     return ap.parse_args()
 
@@ -143,20 +144,59 @@ def kernel_source_hash(kernel="fwd"):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config_name):
-    """DRAM bytes per launch from the committed ncu summary for this workload, if it was taken
-    on the current kernel source; else None."""
-    name = {"bwd": "sparse_mla_bwd_prefill.md"}.get(config_name, f"sparse_mla_fwd_{config_name}.md")
-    path = os.path.join(ROOT, "profiles", name)
-    if not os.path.exists(path):
-        return None
-    text = open(path).read()
-    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def profiled_counters(config_name):
+    """Per-launch ncu counters (DRAM bytes read + written, L2 bytes to the SMs) for this
+    workload's dominant kernel, from the machine-readable file beside the ncu summaries, if
+    they were taken on the current kernel source; else an empty dict."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return {}
+    with open(TRAFFIC_FILE) as f:
+        entry = json.load(f).get(config_name)
     kernel = "bwd" if config_name == "bwd" else "fwd"
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kernel):
-        return None
-    return float(m_bytes.group(1))
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash(kernel):
+        return {}
+    return entry
+
+
+def algorithmic_bytes(w, backward=False):
+    """Compulsory HBM bytes per call (inputs read once, outputs written once) and the L2 -> SM
+    gather bytes (one d_qk row per counted slot)."""
+    s_q, h_q, d_qk = w["q"].shape
+    topk = w["indices"].reshape(s_q, -1).shape[1]
+    counts = W.valid_slot_count(w["indices"], w["s_kv"], w["topk_length"])
+    row = d_qk * 2
+    gather = float(counts.sum()) * row
+    hbm = s_q * h_q * d_qk * 2 + s_q * topk * 4 + s_q * h_q * 8
+    hbm += 0 if w["topk_length"] is None else s_q * 4
+    if w.get("paged"):
+        hbm += gather + w["block_table"].size * 4     # rows come from a pool far larger than L2
+    else:
+        hbm += w["kv"].shape[0] * row                 # the shared KV is read once
+    if backward:
+        # out, dout, lse in; dq (fp32) and dkv (fp32) out
+        hbm += s_q * h_q * w["d_v"] * 4 + s_q * h_q * 4 + s_q * h_q * d_qk * 4 + w["kv"].shape[0] * d_qk * 4
+    else:
+        hbm += s_q * h_q * w["d_v"] * 2
+    return float(hbm), gather
+
+
+def bandwidth(w, config_name, ms, backward=False):
+    """HBM and L2 GB/s of one call: algorithmic bytes and, where the ncu counters for the current
+    kernel source are on file, measured bytes, each over the measured time per call."""
+    hbm, gather = algorithmic_bytes(w, backward)
+    c = profiled_counters(config_name)
+    sec = ms * 1e-3
+    dram = c.get("dram_bytes_per_launch")
+    l2 = c.get("l2_to_sm_bytes_per_launch")
+    return {"hbm_gbs": {"algorithmic": hbm / sec / 1e9, "measured": (dram / sec / 1e9) if dram else None,
+                        "algorithmic_bytes": hbm, "measured_bytes": dram},
+            "l2_gbs": {"algorithmic": gather / sec / 1e9, "measured": (l2 / sec / 1e9) if l2 else None,
+                       "algorithmic_bytes": gather, "measured_bytes": l2},
+            "counters_source": ("profiles/dram_traffic.json (ncu, current kernel source)" if c else
+                                "no ncu counters on file for the current kernel source")}
 
 
 class ClockSampler:
@@ -314,6 +354,60 @@ def cpu_baseline(w, name, budget_s=12.0):
             "sample": f"{done} random rows of the {name} batch ({t_total:.1f} s of fp64 CPU work)"}
 
 
+def decode_fixed_vs_dynamic(smla, torch, dev, stream, flush, n=30):
+    """The paged decode shape (256 requests, h_q 128, d_qk 576, 64-token pages, topk 2048) in its
+    two forms, timed interleaved on the device: dynamic = the first 1024 slots valid, an INT_MAX
+    suffix and topk_length = 1024; fixed = the same 1024 slots, a -1 suffix and no topk_length
+    (FlashMLA PR #216, "Kernel performance" compares exactly these two runs).  The kernel derives
+    the fixed run's length itself, so both should cost the same."""
+    runs = {}
+    for name, dyn in (("dynamic", True), ("fixed", False)):
+        w = W.decode(dynamic=dyn)
+        d = {}
+        for k in ("q", "kv", "indices", "topk_length", "block_table"):
+            a = w.get(k)
+            if a is None:
+                d[k] = None
+                continue
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            if a.dtype == np.uint16:
+                t = t.view(torch.int16).view(torch.bfloat16)
+            d[k] = t.to(dev)
+        runs[name] = (w, d)
+    w0 = runs["dynamic"][0]
+    s_q, h_q = w0["q"].shape[:2]
+    out = torch.empty((s_q, h_q, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((s_q, h_q), dtype=torch.float32, device=dev)
+    mx = torch.empty_like(lse)
+
+    def call(name):
+        w, d = runs[name]
+        smla.sparse_mla_fwd_paged(d["q"], d["kv"], d["block_table"], d["indices"], page_block=w["page_block"],
+                                  s_kv_per_req=w["s_kv_per_req"], s_q_per_req=w["s_q_per_req"],
+                                  topk_length=d["topk_length"], sm_scale=w["sm_scale"], out=out, lse=lse,
+                                  max_logits=mx, stream=stream, n_split=1)
+
+    for _ in range(3):
+        call("dynamic")
+        call("fixed")
+    ms = {"dynamic": [], "fixed": []}
+    for _ in range(n):
+        for name in ("dynamic", "fixed"):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call(name)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms[name].append(a.elapsed_time(b))
+    md, mf = float(np.median(ms["dynamic"])), float(np.median(ms["fixed"]))
+    flops = valid_flops(w0)
+    return {"workload": describe(w0, "decode"), "ms_dynamic": md, "ms_fixed": mf,
+            "fixed_vs_dynamic_gap_pct": 100.0 * (mf - md) / md, "tflops_dynamic": flops / (md * 1e-3) / 1e12,
+            "launches": 6 + 2 * n,
+            "bandwidth": bandwidth(w0, "decode", md)}
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -421,8 +515,15 @@ def main():
                  "padding_gap_pct": 100.0 * (ms_no_len - ms_len) / ms_len,
                  "valid_token_tflop": flops / 1e12}
 
-    # end to end through the C ABI with host buffers: H2D of the inputs, the call, D2H of the
-    # outputs, all inside the timed region
+    # the decode shape's fixed-width run against its dynamic-length run (default run only)
+    decode_leg = None
+    if args.config == "ramp" and not args.skip_decode:
+        decode_leg = decode_fixed_vs_dynamic(smla, torch, dev, stream, flush)
+        launches += decode_leg["launches"]
+
+    # end to end through the C ABI with host buffers: the host-buffer entry point copies each
+    # row chunk's inputs in, runs the forward on it and copies its outputs out, with copies and
+    # compute overlapped on three streams; all of it is inside the timed region
     e2e = None
     if not args.skip_e2e:
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -430,28 +531,45 @@ def main():
         mx_h = torch.empty(mx.shape, dtype=mx.dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
         d2h = sum(t.numel() * t.element_size() for t in (out, lse, mx))
+        copy_streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+        dev_buffers = dict(devt, out=out, lse=lse, max_logits=mx)
         e_ms = []
+
+        def e2e_call():
+            if w.get("paged"):
+                # the paged form has no host-buffer entry: serial copies around the device call
+                for k, v in host.items():
+                    if v is not None:
+                        devt[k].copy_(v, non_blocking=True)
+                call(devt)
+                out_h.copy_(out, non_blocking=True)
+                lse_h.copy_(lse, non_blocking=True)
+                mx_h.copy_(mx, non_blocking=True)
+                return 1
+            smla.sparse_mla_fwd_host(host["q"], host["kv"], host["indices"], host["topk_length"], host["attn_sink"],
+                                     sm_scale=w["sm_scale"], d_v=w["d_v"], out=out_h, lse=lse_h, max_logits=mx_h,
+                                     device=dev, dev_buffers=dev_buffers, n_chunks=args.e2e_chunks, stream=stream,
+                                     copy_streams=copy_streams)
+            return min(args.e2e_chunks, s_q)
+
+        launches_e2e = 0
         for i in range(args.e2e_steps + 2):
             flush.zero_()
             torch.cuda.synchronize(dev)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for k, v in host.items():
-                if v is not None:
-                    devt[k].copy_(v, non_blocking=True)
-            call(devt)
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
-            mx_h.copy_(mx, non_blocking=True)
+            launches_e2e += e2e_call()
             b.record(stream)
             torch.cuda.synchronize(dev)
             if i >= 2:
                 e_ms.append(a.elapsed_time(b))
-        launches_e2e = args.e2e_steps + 2
         e2e_ms = max_over_ranks(float(np.mean(e_ms)), dev)
         e2e = {"value": job_tflops(job_flops, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms,
+               "how": (f"sparse_mla_fwd_host: pinned host buffers, {args.e2e_chunks} row chunks, H2D / compute / "
+                       "D2H overlapped on three streams" if not w.get("paged") else
+                       "serial H2D, device call, D2H on one stream")}
         launches += launches_e2e * launches_per_call
 
     status = smla.sparse_mla_device_status()
@@ -465,7 +583,7 @@ def main():
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (ms_per_step * 1e-3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": profiled_traffic(args.config),
+            "frac": achieved / peak, "traffic": profiled_counters(args.config).get("dram_bytes_per_launch"),
             "peak_source": f"bf16_tflops burst ({src})", "kernel": "sparse_mla_fwd_kernel"}
     base = PAGES_B200_TFLOPS.get((args.config, bool(args.with_len)))
     line = {
@@ -485,6 +603,9 @@ def main():
         "device_status": status,
     }
     line.update(extra)
+    line["bandwidth"] = bandwidth(w, args.config, ms_per_step)
+    if decode_leg is not None:
+        line["decode_fixed_vs_dynamic"] = decode_leg
     if e2e is not None:
         line["e2e"] = e2e
     if not args.skip_cpu and world == 1:
@@ -590,10 +711,11 @@ def main_bwd(args, w, world, rank, local, dev, barrier):
                    "l2": "flushed (256 MB write) between timed iterations",
                    "pct_of_bf16_peak": 100.0 * achieved / peak},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic("bwd"),
+                     "frac": achieved / peak, "traffic": profiled_counters("bwd").get("dram_bytes_per_launch"),
                      "peak_source": f"bf16_tflops burst ({src})", "kernel": "sparse_mla_bwd_kernel"},
         "clocks": clocks, "gpu_launches": steps, "device_status": status,
     }
+    line["bandwidth"] = bandwidth(w, "bwd", ms_per_step, backward=True)
     if e2e is not None:
         line["e2e"] = e2e
     if not args.skip_cpu and world == 1:

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 3
+#define SMLA_ABI_VERSION 4
 
 typedef struct CUstream_st* smla_stream_t; /* a cudaStream_t; NULL = legacy default stream */
 
@@ -81,13 +81,15 @@ smla_status sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices
  * per-request top-k token positions in a cache of 64-token pages).
  *   kv_pool      [pool_rows, 1, d_qk] bf16; pool_rows = number of pages * page_block
  *   block_table  [s_q / s_q_per_req, max_blocks] int32: page id of each page_block-token
- *                block of every request; entries must name pages inside the pool
+ *                block of every request; a negative entry marks an unmapped page
  *   seqlens_k    [s_q / s_q_per_req] int32 KV length of each request, or NULL to use
  *                s_kv_per_req for all requests
  *   indices      [s_q, 1, topk] int32 token positions within the row's request
  * Query row t belongs to request t / s_q_per_req (s_q must be a multiple of s_q_per_req).
  * Position p of request b is read from pool row block_table[b][p / page_block] * page_block
- * + p % page_block, and counts iff 0 <= p < seqlens_k[b] and p / page_block < max_blocks.
+ * + p % page_block, and counts iff 0 <= p < seqlens_k[b], p / page_block < max_blocks, the
+ * table entry is >= 0 and the row is < pool_rows; any other position is an invalid slot and is
+ * never used as an address (FlashMLA PR #216, "Summary").
  * All other arguments and outputs are as in sparse_mla_fwd.
  */
 smla_status sparse_mla_fwd_paged(const void* q, const void* kv_pool, int64_t pool_rows,
@@ -155,6 +157,35 @@ smla_status sparse_mla_fwd_paged_splitkv_static(
     const int32_t* indices, const int32_t* topk_length, const float* attn_sink, float sm_scale, int d_v,
     void* out, float* lse, float* max_logits, int64_t s_q, int h_q, int d_qk, int topk, int n_split,
     smla_stream_t stream);
+
+/*
+ * End-to-end form of sparse_mla_fwd for inputs and outputs that live in HOST memory: the
+ * host -> device copies of the inputs, the forward and the device -> host copies of the
+ * outputs, pipelined over row chunks so that the copies of one chunk overlap the compute of
+ * another.  Rows are independent, so the results are bit-identical to one sparse_mla_fwd call.
+ *   *_host       host buffers with the layouts of sparse_mla_fwd (inputs read, outputs
+ *                written); page-locked (pinned) memory is needed for the copies to overlap
+ *   *_dev        caller-owned device buffers of the full sizes, with the alignment rules of
+ *                sparse_mla_fwd; the inputs are copied into them and the outputs computed in
+ *                them.  topk_length_dev / attn_sink_dev are NULL exactly when their host
+ *                counterparts are (kv_host / kv_dev may be NULL only when s_kv == 0)
+ *   n_chunks     1 .. 64: the rows are cut into n_chunks ranges of ceil(s_q / n_chunks) rows
+ *   stream       the compute stream; when it has finished, every output copy has finished
+ *   copy_in      stream of the host -> device copies (kv and attn_sink first, then each chunk)
+ *   copy_out     stream of the device -> host copies
+ * The copies start after the work already queued on `stream`, so the call is ordered on
+ * `stream` as a whole.  The three streams are ordered with CUDA events that the call creates
+ * and releases (no memory is allocated).  The call only enqueues work; synchronise `stream` before reading
+ * the host outputs.  Every argument is checked before anything is enqueued; SMLA_ERR_LAUNCH
+ * (a failed copy, event or launch) can come after earlier chunks were enqueued.
+ */
+smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_host, const int32_t* indices_host,
+                                const int32_t* topk_length_host, const float* attn_sink_host, float sm_scale,
+                                int d_v, void* out_host, float* lse_host, float* max_logits_host, int64_t s_q,
+                                int64_t s_kv, int h_q, int d_qk, int topk, void* q_dev, void* kv_dev,
+                                int32_t* indices_dev, int32_t* topk_length_dev, float* attn_sink_dev, void* out_dev,
+                                float* lse_dev, float* max_logits_dev, int n_chunks, smla_stream_t stream,
+                                smla_stream_t copy_in, smla_stream_t copy_out);
 
 /*
  * Reads (and, when reset != 0, clears) the device-side status word that kernels set when one

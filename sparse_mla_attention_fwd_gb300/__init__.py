@@ -25,7 +25,8 @@ import torch
 from ._native import EXPORTED, SmlaError, load_library, status_string
 from .native_build import LIB_PATH, build as build_library
 
-__all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_fwd_paged_splitkv_static", "auto_splits",
+__all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_fwd_paged_splitkv_static", "sparse_mla_fwd_host",
+           "auto_splits",
            "sparse_mla_bwd", "sparse_mla_device_status",
            "sparse_mla_status_string", "SmlaError", "load_library", "build_library", "LIB_PATH"]
 
@@ -69,6 +70,68 @@ def _outputs(q, h_q, d_v, out, lse, max_logits):
     if tuple(out.shape) != (s_q, h_q, d_v) or tuple(lse.shape) != (s_q, h_q) \
             or tuple(max_logits.shape) != (s_q, h_q):
         raise ValueError("output tensors have the wrong shape")
+    return out, lse, max_logits
+
+
+def _host(t, name, dtype):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} host tensor")
+
+
+def sparse_mla_fwd_host(q, kv, indices, topk_length=None, attn_sink=None, sm_scale=None, d_v=512,
+                        out=None, lse=None, max_logits=None, device=None, dev_buffers=None, n_chunks=8,
+                        stream=None, copy_streams=None):
+    """The forward for host tensors (pinned for the copies to overlap), end to end: the C entry
+    copies each row chunk's inputs to the device, runs the forward on it and copies its outputs
+    back, with the copies of one chunk overlapping the compute of another.  Outputs are host
+    tensors (pinned, allocated here when not given).  `dev_buffers` (a dict with the keys q, kv,
+    indices, topk_length, attn_sink, out, lse, max_logits) and `copy_streams` (two streams: in,
+    out) are allocated here when not given.  The call is asynchronous on `stream`: synchronise
+    it before reading the outputs."""
+    lib = load_library()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _host(q, "q", torch.bfloat16)
+    _host(kv, "kv", torch.bfloat16)
+    _host(indices, "indices", torch.int32)
+    _host(topk_length, "topk_length", torch.int32)
+    _host(attn_sink, "attn_sink", torch.float32)
+    s_q, h_q, d_qk = q.shape
+    s_kv = kv.shape[0]
+    topk = indices.shape[-1]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d_qk)
+    if out is None:
+        out = torch.empty((s_q, h_q, d_v), dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32).pin_memory()
+    if max_logits is None:
+        max_logits = torch.empty((s_q, h_q), dtype=torch.float32).pin_memory()
+    _host(out, "out", torch.bfloat16)
+    _host(lse, "lse", torch.float32)
+    _host(max_logits, "max_logits", torch.float32)
+    if dev_buffers is None:
+        def like(t, shape=None):
+            return None if t is None else torch.empty(t.shape if shape is None else shape, dtype=t.dtype, device=dev)
+        dev_buffers = dict(q=like(q), kv=like(kv), indices=like(indices), topk_length=like(topk_length),
+                           attn_sink=like(attn_sink), out=like(out), lse=like(lse), max_logits=like(max_logits))
+    d = dev_buffers
+    for k, dt in (("q", torch.bfloat16), ("kv", torch.bfloat16), ("indices", torch.int32),
+                  ("topk_length", torch.int32), ("attn_sink", torch.float32), ("out", torch.bfloat16),
+                  ("lse", torch.float32), ("max_logits", torch.float32)):
+        _check(d.get(k), "dev_buffers[" + k + "]", dt, dev)
+    if copy_streams is None:
+        copy_streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    with torch.cuda.device(dev):
+        rc = lib.sparse_mla_fwd_host(
+            _ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length), _ptr(attn_sink), float(sm_scale), int(d_v),
+            _ptr(out), _ptr(lse), _ptr(max_logits), int(s_q), int(s_kv), int(h_q), int(d_qk), int(topk),
+            _ptr(d["q"]), _ptr(d["kv"]), _ptr(d["indices"]), _ptr(d.get("topk_length")), _ptr(d.get("attn_sink")),
+            _ptr(d["out"]), _ptr(d["lse"]), _ptr(d["max_logits"]), int(n_chunks), _stream_handle(stream, dev),
+            copy_streams[0].cuda_stream, copy_streams[1].cuda_stream)
+    if rc != 0:
+        raise SmlaError(rc, "sparse_mla_fwd_host")
     return out, lse, max_logits
 
 

@@ -17,7 +17,7 @@ STATUS_NAMES = {0: "SMLA_OK", 1: "SMLA_ERR_NULL_PTR", 2: "SMLA_ERR_BAD_SHAPE",
                 6: "SMLA_ERR_TENSOR_MAP", 7: "SMLA_ERR_WORKSPACE"}
 EXPORTED = ("sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_splitkv_workspace_size",
             "sparse_mla_fwd_splitkv", "sparse_mla_fwd_paged_splitkv", "sparse_mla_fwd_paged_splitkv_static",
-            "sparse_mla_selftest_wait_timeout", "sparse_mla_device_status",
+            "sparse_mla_fwd_host", "sparse_mla_selftest_wait_timeout", "sparse_mla_device_status",
             "sparse_mla_status_string", "sparse_mla_abi_version", "sparse_mla_bwd")
 
 _lock = threading.Lock()
@@ -60,6 +60,9 @@ def load_library(path: str | None = None):
         lib.sparse_mla_fwd_paged_splitkv_static.restype = I32
         lib.sparse_mla_fwd_paged_splitkv_static.argtypes = [P, P, I64, P, I32, I32, P, I64, I32, P, P, P, F32,
                                                             I32, P, P, P, I64, I32, I32, I32, I32, P]
+        lib.sparse_mla_fwd_host.restype = I32
+        lib.sparse_mla_fwd_host.argtypes = [P, P, P, P, P, F32, I32, P, P, P, I64, I64, I32, I32, I32,
+                                            P, P, P, P, P, P, P, P, I32, P, P, P]
         lib.sparse_mla_selftest_wait_timeout.restype = I32
         lib.sparse_mla_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
         lib.sparse_mla_device_status.restype = I32

@@ -50,6 +50,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -86,8 +87,10 @@ constexpr uint32_t kTmemVT = 384;      // V^T of value chunks 0-1: 2 buffers x 2
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only when the running max grows by > 2^8
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // every device wait gives up after 2 s
 
-enum : uint32_t { kFirstBlock = 1u, kLastBlock = 2u };
+// kEndOfWork marks the ring entry after the last block of the CTA's last work unit.
+enum : uint32_t { kFirstBlock = 1u, kLastBlock = 2u, kEndOfWork = 4u };
 
 __device__ int g_device_status = 0;    // SMLA_ERR_DEVICE_TIMEOUT once any wait gave up
 
@@ -140,7 +143,6 @@ struct FwdParams {
   int page_block;
   int s_q_per_req;
   int64_t pool_rows;           // rows the KV tensor map covers
-  uint64_t wait_limit_ns;
   // split-KV: each item's slot list is cut into n_split ranges, one work unit each, whose
   // partial results go to part_o [unit][64 heads][512] (unnormalised O) and part_stats
   // [unit][3][64] (exponent offset m in log2 units, sum l, max of sm_scale * q.k)
@@ -154,7 +156,7 @@ struct BlockDesc {
   int32_t rows[kBlockN];       // TMA row coordinate per slot, -1 when the slot does not count
   uint32_t mask[2];            // validity bits of slots 0-31 / 32-63
   int32_t item;                // work item this block belongs to
-  uint32_t flags;              // kFirstBlock | kLastBlock
+  uint32_t flags;              // kFirstBlock | kLastBlock, or kEndOfWork alone
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -254,9 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   volatile int* abort = &abort_flag;
-  const uint64_t lim = p.wait_limit_ns;
-  // work units of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...  A unit is an item
-  // (token, 64-head group) or, with SPLIT, an (item, slot range) pair.
+  constexpr uint64_t lim = kDefaultWaitLimitNs;
+  // Work units: an item (token, 64-head group) or, with SPLIT, an (item, slot range) pair.  One
+  // CTA per SM walks the units blockIdx.x, blockIdx.x + gridDim.x, ...  The scheduler warp
+  // publishes their blocks in that order, followed by an end-of-work entry; every role but the
+  // QK issuer simply follows the block ring until that entry.
   const int64_t n_units = SPLIT ? p.n_items * p.n_split : p.n_items;
   const int64_t n_my_items = n_units > blockIdx.x ? (n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
   auto item_of_unit = [&](int64_t u) -> int64_t { return SPLIT ? u / p.n_split : u; };
@@ -320,9 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used[2] = {-INFINITY, -INFINITY};    // running exponent offsets (log2 units)
     float s_max[2] = {-INFINITY, -INFINITY};     // running max of raw q.k
     float l_sum[2] = {0.f, 0.f};
-    int64_t b = 0;
-    for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-      for (bool more = true; more && !*abort; ++b) {
+    for (int64_t b = 0; !*abort; ++b) {
+      {
         const int r = static_cast<int>(b % kRing);
         const int sb = static_cast<int>(b & 1);
         wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
@@ -331,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t item = ring[r].item;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_ring_empty[r]));
-        more = (flags & kLastBlock) == 0;
+        if (flags & kEndOfWork) break;
+        const bool more = (flags & kLastBlock) == 0;
         const bool first = (flags & kFirstBlock) != 0;
         if (first) {
 #pragma unroll
@@ -558,8 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       int64_t b = 0;
-      for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-        const int64_t unit = blockIdx.x + i * gridDim.x;
+      for (int64_t unit = blockIdx.x; unit < n_units && !*abort; unit += gridDim.x) {
         const int64_t item = unit;   // what the ring carries: the unit (the item itself unless SPLIT)
         const int64_t t = item_of_unit(unit) / p.n_groups;
         const int32_t* idx_row = p.indices + t * static_cast<int64_t>(p.topk);
@@ -576,14 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int last = -1, cnt = 0;
         if constexpr (PAGED) {
           // Decode-shaped work has few blocks per CTA, so the scan's load latency is exposed:
-          // pull the next row's list into L2 and keep eight 32-slot chunks of loads in flight.
-          // (On the prefill paths, which are throughput-bound, this form measured slower.)
-          if (i + 1 < n_my_items) {
-            const int64_t tn = item_of_unit(unit + gridDim.x) / p.n_groups;
-            const char* nrow = reinterpret_cast<const char*>(p.indices + tn * static_cast<int64_t>(p.topk));
-            for (int off = lane * 128; off < p.topk * 4; off += 32 * 128)
-              asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + off));
-          }
+          // keep eight 32-slot chunks of loads in flight.  (On the prefill paths, which are
+          // throughput-bound, this form measured slower.)
           for (int j0 = 0; j0 < Lr; j0 += 8 * 32) {
             int vals[8];
 #pragma unroll
@@ -633,47 +630,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             publish(b, m[0], m[1], (k == 0 ? kFirstBlock : 0u) | (k == nblk - 1 ? kLastBlock : 0u), item);
           }
-          continue;
-        }
-        // packing pass over [0, L): the indices were just read and come from L1
-        const int64_t b0 = b;
-        int count = 0;               // counted slots packed so far
-        int64_t acquired = b0 - 1;   // last block whose ring slot is held
-        int64_t published = b0;      // next block to publish
-        for (int j0 = 0; j0 < L && !*abort; j0 += 32) {
-          const int slot = j0 + lane;
-          int coord = -1;
-          if (slot < L) {
-            const int v = __ldg(idx_row + slot);
-            if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+        } else {
+          // packing pass over [0, L): the indices were just read and come from L1
+          const int64_t b0 = b;
+          int count = 0;               // counted slots packed so far
+          int64_t acquired = b0 - 1;   // last block whose ring slot is held
+          int64_t published = b0;      // next block to publish
+          for (int j0 = 0; j0 < L && !*abort; j0 += 32) {
+            const int slot = j0 + lane;
+            int coord = -1;
+            if (slot < L) {
+              const int v = __ldg(idx_row + slot);
+              if (slot_ok<PAGED>(p, v, kv_len)) coord = kv_row_of<PAGED>(p, t, v);
+            }
+            const uint32_t bal = __ballot_sync(0xffffffffu, coord >= 0);
+            if (bal == 0u) continue;
+            const int n = __popc(bal);
+            const int64_t newest = b0 + (count + n - 1) / kBlockN;   // block of the newest slot
+            while (acquired < newest) acquire(++acquired);
+            if (coord >= 0) {
+              const int pos = count + __popc(bal & lanes_below);
+              ring[(b0 + pos / kBlockN) % kRing].rows[pos % kBlockN] = coord;
+            }
+            count += n;
+            __syncwarp();
+            // every block before the newest one is full and has a successor
+            for (; published < newest; ++published)
+              publish(published, 0xffffffffu, 0xffffffffu, published == b0 ? kFirstBlock : 0u, item);
           }
-          const uint32_t bal = __ballot_sync(0xffffffffu, coord >= 0);
-          if (bal == 0u) continue;
-          const int n = __popc(bal);
-          const int64_t newest = b0 + (count + n - 1) / kBlockN;   // block of the newest slot
-          while (acquired < newest) acquire(++acquired);
-          if (coord >= 0) {
-            const int pos = count + __popc(bal & lanes_below);
-            ring[(b0 + pos / kBlockN) % kRing].rows[pos % kBlockN] = coord;
-          }
-          count += n;
+          // the block that holds the row's last counted slot (or one empty block) closes the item
+          if (count == 0) acquire(++acquired);
+          const int64_t lastb = b0 + (count > 0 ? (count - 1) / kBlockN : 0);
+          const int fill = count - static_cast<int>(lastb - b0) * kBlockN;   // 0..64 slots used
+          const int rl = static_cast<int>(lastb % kRing);
+          for (int e = fill + lane; e < kBlockN; e += 32) ring[rl].rows[e] = -1;
+          const uint32_t m0 = fill >= 32 ? 0xffffffffu : ((1u << fill) - 1u);
+          const uint32_t m1 = fill >= 64 ? 0xffffffffu : (fill > 32 ? ((1u << (fill - 32)) - 1u) : 0u);
           __syncwarp();
-          // every block before the newest one is full and has a successor
-          for (; published < newest; ++published)
-            publish(published, 0xffffffffu, 0xffffffffu, published == b0 ? kFirstBlock : 0u, item);
+          publish(lastb, m0, m1, (lastb == b0 ? kFirstBlock : 0u) | kLastBlock, item);
+          b = lastb + 1;
         }
-        // the block that holds the row's last counted slot (or one empty block) closes the item
-        if (count == 0) acquire(++acquired);
-        const int64_t lastb = b0 + (count > 0 ? (count - 1) / kBlockN : 0);
-        const int fill = count - static_cast<int>(lastb - b0) * kBlockN;   // 0..64 slots used
-        const int rl = static_cast<int>(lastb % kRing);
-        for (int e = fill + lane; e < kBlockN; e += 32) ring[rl].rows[e] = -1;
-        const uint32_t m0 = fill >= 32 ? 0xffffffffu : ((1u << fill) - 1u);
-        const uint32_t m1 = fill >= 64 ? 0xffffffffu : (fill > 32 ? ((1u << (fill - 32)) - 1u) : 0u);
-        __syncwarp();
-        publish(lastb, m0, m1, (lastb == b0 ? kFirstBlock : 0u) | kLastBlock, item);
-        b = lastb + 1;
       }
+      // every role stops at this entry
+      acquire(b);
+      publish(b, 0u, 0u, kEndOfWork, -1);
     } else if (warp < 2 || warp == 3 || warp == 8 || warp == 9 || warp >= kVtWarp0) {
       // ======================================================== gather (+ V^T copies)
       // TMA issue throughput grows with the number of issuing warps, so the 16 x (chunks of a
@@ -734,15 +734,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         SMLA_TRACE_EVENT_IF(q == 0 && lane == 0, j, kTrVtEnd);
       };
       int64_t b = 0;
-      for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-        for (bool more = true; more && !*abort; ++b) {
+      for (; !*abort; ++b) {
+        {
           const int r = static_cast<int>(b % kRing);
           const int s = static_cast<int>(b & 1);
           wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
-          more = (ring[r].flags & kLastBlock) == 0;
+          const uint32_t fl = ring[r].flags;
           const int4 rr = *reinterpret_cast<const int4*>(&ring[r].rows[4 * grp]);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bar_ring_empty[r]));
+          if (fl & kEndOfWork) break;
 #pragma unroll
           for (int g = 0; g < kGroups; ++g) {
             const int c0 = 2 * g;
@@ -842,19 +843,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc_pv = make_idesc_bf16(128, kGroupHeads, true, false);
         constexpr uint32_t idesc_pv_ts = make_idesc_bf16(128, kGroupHeads, false, false);
         const uint32_t kv_base = smem_u32(sKV);
-        int64_t b = 0;
-        for (int64_t i = 0; i < n_my_items && !*abort; ++i) {
-          for (bool more = true; more && !*abort; ++b) {
+        uint32_t units_started = 0;
+        for (int64_t b = 0; !*abort; ++b) {
+          {
             const int r = static_cast<int>(b % kRing);
             const int sb = static_cast<int>(b & 1);
             wait_or_flag(smem_u32(&bar_ring_full[r]), (b / kRing) & 1, abort, lim);
             const uint32_t fl = ring[r].flags;
             mbar_arrive(smem_u32(&bar_ring_empty[r]));
-            more = (fl & kLastBlock) == 0;
+            if (fl & kEndOfWork) break;
             const bool first = (fl & kFirstBlock) != 0;
             wait_or_flag(smem_u32(&bar_p_full[sb]), (b >> 1) & 1, abort, lim);
-            // the epilogue of the previous item has read all of O^T
-            if (first && i > 0) wait_or_flag(smem_u32(&bar_o_free), (i - 1) & 1, abort, lim);
+            // the epilogue of the previous unit has read all of O^T
+            if (first) {
+              if (units_started > 0) wait_or_flag(smem_u32(&bar_o_free), (units_started - 1) & 1, abort, lim);
+              ++units_started;
+            }
             tc_fence_after();
             SMLA_TRACE_EVENT(b, kTrPvIssue);
             // descriptor start addresses advance in 16-byte units (low 14 bits)
@@ -912,6 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // and a head without any counted slot gets O = 0, lse = +inf, max_logits = -inf.  With one
 // range this is the same arithmetic as the single-pass epilogue.
 constexpr int kMaxSplit = 64;
+constexpr int kMaxHostChunks = 64;      // row chunks of the host-buffer entry point
 constexpr int kMergeHeads = 1;       // heads per merge CTA (many small CTAs: loads in flight)
 constexpr int kMergeThreads = 128;   // four value columns d per thread (float4)
 
@@ -1044,10 +1049,10 @@ smla_status launch_one(const CUtensorMap& qm, const CUtensorMap& kvm, const FwdP
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return SMLA_ERR_LAUNCH;
-  const int sms = sm_count();
-  if (sms <= 0) return SMLA_ERR_LAUNCH;
   // persistent: one CTA per SM (the shared-memory footprint admits only one), work units
   // assigned round-robin
+  const int sms = sm_count();
+  if (sms <= 0) return SMLA_ERR_LAUNCH;
   const int64_t units = SPLIT ? p.n_items * p.n_split : p.n_items;
   const int64_t grid = units < sms ? units : sms;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(qm, kvm, p);
@@ -1099,8 +1104,6 @@ smla_status check_common(const void* q, const void* kv, const int32_t* indices, 
     return SMLA_ERR_MISALIGNED;
   return SMLA_OK;
 }
-
-constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 
 // the backward kernel and its host side share the helpers above
 #include "sparse_mla_bwd.cuh"
@@ -1176,7 +1179,6 @@ smla_status fwd_flat(const void* q, const void* kv, const int32_t* indices, cons
   p.page_block = 1;
   p.max_blocks = 1;
   p.pool_rows = s_kv;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
   return dispatch<false>(d_qk, topk_length != nullptr, qm, kvm, p, stream);
 }
 
@@ -1222,7 +1224,6 @@ smla_status fwd_paged(const void* q, const void* kv_pool, int64_t pool_rows, con
   p.page_block = page_block;
   p.s_q_per_req = s_q_per_req;
   p.pool_rows = pool_rows;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
   return dispatch<true>(d_qk, topk_length != nullptr, qm, kvm, p, stream);
 }
 
@@ -1281,6 +1282,87 @@ smla_status sparse_mla_fwd_paged_splitkv_static(
   return fwd_paged(q, kv_pool, pool_rows, block_table, max_blocks, page_block, seqlens_k, s_kv_per_req,
                    s_q_per_req, indices, topk_length, attn_sink, sm_scale, d_v, out, lse, max_logits,
                    s_q, h_q, d_qk, topk, n_split, scratch, kStaticScratchBytes, stream);
+}
+
+smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_host, const int32_t* indices_host,
+                                const int32_t* topk_length_host, const float* attn_sink_host, float sm_scale,
+                                int d_v, void* out_host, float* lse_host, float* max_logits_host, int64_t s_q,
+                                int64_t s_kv, int h_q, int d_qk, int topk, void* q_dev, void* kv_dev,
+                                int32_t* indices_dev, int32_t* topk_length_dev, float* attn_sink_dev, void* out_dev,
+                                float* lse_dev, float* max_logits_dev, int n_chunks, cudaStream_t stream,
+                                cudaStream_t copy_in, cudaStream_t copy_out) {
+  // every argument is checked before anything is enqueued
+  if (n_chunks < 1 || n_chunks > kMaxHostChunks) return SMLA_ERR_BAD_SHAPE;
+  if (s_kv < 0 || s_kv > INT32_MAX) return SMLA_ERR_BAD_SHAPE;
+  smla_status st = check_common(q_dev, s_kv > 0 ? kv_dev : q_dev, indices_dev, out_dev, lse_dev, max_logits_dev,
+                                s_q, h_q, d_qk, d_v, topk, sm_scale);
+  if (st != SMLA_OK || s_q == 0) return st;
+  if (!q_host || !indices_host || !out_host || !lse_host || !max_logits_host || (s_kv > 0 && !kv_host))
+    return SMLA_ERR_NULL_PTR;
+  if ((topk_length_host == nullptr) != (topk_length_dev == nullptr) ||
+      (attn_sink_host == nullptr) != (attn_sink_dev == nullptr))
+    return SMLA_ERR_NULL_PTR;
+  if ((attn_sink_dev && !aligned4(attn_sink_dev)) || (topk_length_dev && !aligned4(topk_length_dev)))
+    return SMLA_ERR_MISALIGNED;
+  const int64_t rows_per = (s_q + n_chunks - 1) / n_chunks;
+  const int chunks = static_cast<int>((s_q + rows_per - 1) / rows_per);
+  // events order the three streams: inputs of chunk i -> its kernel -> its outputs
+  cudaEvent_t ev[2 * kMaxHostChunks + 3];
+  const int n_ev = 2 * chunks + 3;
+  for (int e = 0; e < n_ev; ++e) {
+    if (cudaEventCreateWithFlags(&ev[e], cudaEventDisableTiming) != cudaSuccess) {
+      for (int k = 0; k < e; ++k) cudaEventDestroy(ev[k]);
+      return SMLA_ERR_LAUNCH;
+    }
+  }
+  cudaEvent_t ev_kv = ev[0], ev_done = ev[1], ev_start = ev[2];
+  auto ev_in = [&](int i) { return ev[3 + 2 * i]; };
+  auto ev_k = [&](int i) { return ev[4 + 2 * i]; };
+  const size_t q_row = static_cast<size_t>(h_q) * d_qk * 2, o_row = static_cast<size_t>(h_q) * d_v * 2;
+  const size_t s_row = static_cast<size_t>(h_q) * sizeof(float), i_row = static_cast<size_t>(topk) * 4;
+  auto h2d = [&](void* dst, const void* src, size_t n) {
+    return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, copy_in) == cudaSuccess;
+  };
+  auto d2h = [&](void* dst, const void* src, size_t n) {
+    return cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, copy_out) == cudaSuccess;
+  };
+  // the copies come after the work already queued on `stream` (which may still read the
+  // device buffers), as if the whole call ran on `stream`
+  bool ok = cudaEventRecord(ev_start, stream) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(copy_in, ev_start, 0) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(copy_out, ev_start, 0) == cudaSuccess;
+  // the inputs every chunk shares, then each chunk's rows
+  ok = ok && h2d(kv_dev, kv_host, static_cast<size_t>(s_kv) * d_qk * 2);
+  if (attn_sink_dev) ok = ok && h2d(attn_sink_dev, attn_sink_host, s_row);
+  ok = ok && cudaEventRecord(ev_kv, copy_in) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(stream, ev_kv, 0) == cudaSuccess;
+  for (int i = 0; i < chunks && ok && st == SMLA_OK; ++i) {
+    const int64_t r0 = i * rows_per, n = std::min(rows_per, s_q - r0);
+    ok = ok && h2d(static_cast<uint8_t*>(q_dev) + r0 * q_row, static_cast<const uint8_t*>(q_host) + r0 * q_row,
+                   n * q_row);
+    ok = ok && h2d(indices_dev + r0 * topk, indices_host + r0 * topk, n * i_row);
+    if (topk_length_dev) ok = ok && h2d(topk_length_dev + r0, topk_length_host + r0, n * 4);
+    ok = ok && cudaEventRecord(ev_in(i), copy_in) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(stream, ev_in(i), 0) == cudaSuccess;
+    if (!ok) break;
+    // the rows of one chunk are an independent forward call: the same bits as one call on all
+    st = fwd_flat(static_cast<uint8_t*>(q_dev) + r0 * q_row, kv_dev, indices_dev + r0 * topk,
+                  topk_length_dev ? topk_length_dev + r0 : nullptr, attn_sink_dev, sm_scale, d_v,
+                  static_cast<uint8_t*>(out_dev) + r0 * o_row, lse_dev + r0 * h_q, max_logits_dev + r0 * h_q, n,
+                  s_kv, h_q, d_qk, topk, 1, nullptr, 0, stream);
+    ok = ok && cudaEventRecord(ev_k(i), stream) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(copy_out, ev_k(i), 0) == cudaSuccess;
+    ok = ok && d2h(static_cast<uint8_t*>(out_host) + r0 * o_row, static_cast<const uint8_t*>(out_dev) + r0 * o_row,
+                   n * o_row);
+    ok = ok && d2h(lse_host + r0 * h_q, lse_dev + r0 * h_q, n * s_row);
+    ok = ok && d2h(max_logits_host + r0 * h_q, max_logits_dev + r0 * h_q, n * s_row);
+  }
+  // the caller's stream completes only after the last copy out
+  ok = ok && cudaEventRecord(ev_done, copy_out) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(stream, ev_done, 0) == cudaSuccess;
+  for (int e = 0; e < n_ev; ++e) cudaEventDestroy(ev[e]);   // released once they complete
+  if (st != SMLA_OK) return st;
+  return ok ? SMLA_OK : SMLA_ERR_LAUNCH;
 }
 
 smla_status sparse_mla_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.sparse_mla_abi_version() == 3
+    assert lib.sparse_mla_abi_version() == 4
     for code in range(8):
         s = smla.sparse_mla_status_string(code)
         assert s and s != "unknown status"
@@ -133,3 +133,19 @@ def call_bwd(lib, q=FAKE, kv=FAKE, out=FAKE, dout=FAKE, idx=FAKE, tl=None, sink=
 ])
 def test_bwd_rejects_bad_arguments_before_any_launch(lib, kw, code):
     assert call_bwd(lib, **kw) == code
+
+
+def test_host_entry_rejects_bad_arguments_before_any_copy(lib):
+    f = lib.sparse_mla_fwd_host
+
+    def call(q_h=FAKE, kv_h=FAKE, idx_h=FAKE, tl_h=None, sink_h=None, out_h=FAKE, tl_d=None, sink_d=None,
+             n_chunks=4, s_q=16, q_d=FAKE):
+        return f(q_h, kv_h, idx_h, tl_h, sink_h, ctypes.c_float(0.04), 512, out_h, FAKE, FAKE, s_q, 100, 64, 576,
+                 32, q_d, FAKE, FAKE, tl_d, sink_d, FAKE, FAKE, FAKE, n_chunks, None, None, None)
+
+    assert call(n_chunks=0) == 2 and call(n_chunks=65) == 2
+    assert call(q_h=None) == 1 and call(kv_h=None) == 1 and call(out_h=None) == 1
+    assert call(tl_h=FAKE) == 1 and call(tl_d=FAKE) == 1          # host and device must match
+    assert call(sink_h=FAKE) == 1
+    assert call(q_d=FAKE + 8) == 3
+    assert call(s_q=0, q_h=None, out_h=None) == 0                   # no rows: nothing is inspected

@@ -98,8 +98,9 @@ def test_bwd_dq_is_deterministic_and_dkv_stable():
 def test_bwd_full_size_sampled_rows_and_column_sums():
     """The backward on the bench shape (s_q 4096, s_kv 32768, h_q 64, d_qk 576, topk 2048) in the
     launch configuration bench.py times.  dq of a row depends on that row alone, so sampled rows
-    are checked against the oracle one by one.  dkv is checked through a property that holds at
-    any size: without a sink, sum_s dS_s = D (1 - sum_s p_s) = 0 for every (row, head), so the
+    are checked against the oracle one by one.  dkv is checked element by element on sampled kv
+    rows (against the oracle over every query row that selects them) and, at every column,
+    through a property that holds at any size: without a sink, sum_s dS_s = D (1 - sum_s p_s) = 0 for every (row, head), so the
     column sums of dkv are sum_{t,h} dO[t,h,d] on the value columns and 0 on the rope columns."""
     w = W.bwd_prefill()
     dout = W.dout_for(w)
@@ -109,6 +110,13 @@ def test_bwd_full_size_sampled_rows_and_column_sums():
     idx = w["indices"].reshape(w["q"].shape[0], -1)
     rq, _, _ = oracle.sparse_mla_bwd(w["q"][rows], w["kv"], dout[rows], idx[rows], None, None, w["sm_scale"])
     _close(dq[rows], rq, "dq (sampled rows)")
+    # dkv element by element on sampled kv rows: the oracle over every query row that selects
+    # one of them gives those rows' complete gradient
+    kv_rows = np.array([5, 12345, 20000, w["kv"].shape[0] - 1])
+    sel = np.where(np.isin(idx, kv_rows).any(axis=1))[0]
+    assert len(sel) > 100
+    _, rkv, _ = oracle.sparse_mla_bwd(w["q"][sel], w["kv"], dout[sel], idx[sel], None, None, w["sm_scale"])
+    _close(dkv[kv_rows], rkv[kv_rows], "dkv (sampled kv rows, every selecting row)")
     d_v = w["d_v"]
     ref = np.zeros(w["q"].shape[2])
     ref[:d_v] = oracle.bf16_bits_to_f64(dout).sum(axis=(0, 1))

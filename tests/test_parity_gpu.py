@@ -116,22 +116,28 @@ def test_single_valid_slot_is_bit_exact():
 
 
 # ---------------------------------------------------------------- full-size configurations
-SAMPLE = 48
+# At the benchmark sizes every row is compared with the oracle (C3: 1024 rows plus fixed ones),
+# in chunks of rows so that the fp64 reference stays small; each chunk must meet the bar.
+CHUNK = 1024
+_ORACLE_CACHE = {}
 
 
-def _sampled_rows(s_q, extra=()):
-    rng = np.random.default_rng(1234)
-    rows = set(rng.choice(s_q, size=min(SAMPLE, s_q), replace=False).tolist())
-    rows.update([0, 1, s_q - 1])
-    rows.update(int(r) for r in extra)
-    return np.array(sorted(rows), np.int64)
+def _oracle_rows(w, key, rows):
+    """Oracle outputs for `rows` of workload `key`, cached across tests that share the inputs
+    (the ramp runs with and without topk_length have the same expected output)."""
+    ck = (key, rows.tobytes())
+    if ck not in _ORACLE_CACHE:
+        _ORACLE_CACHE[ck] = run_oracle(w, rows=rows)
+    return _ORACLE_CACHE[ck]
 
 
-def _check_full(w, what, extra_rows=()):
+def _check_full(w, what, key, rows=None):
     s_q = w["q"].shape[0]
     gpu = run_gpu(w)
-    rows = _sampled_rows(s_q, extra_rows)
-    assert_parity(to_np(gpu, rows), run_oracle(w, rows=rows), what)
+    rows = np.arange(s_q, dtype=np.int64) if rows is None else rows
+    for c0 in range(0, len(rows), CHUNK):
+        r = rows[c0:c0 + CHUNK]
+        assert_parity(to_np(gpu, r), _oracle_rows(w, key, r), f"{what} rows {r[0]}..{r[-1]}")
     # properties at every row: finite where the row has a counted slot, exact empties elsewhere
     counts = W.valid_slot_count(w["indices"], w["s_kv"], w["topk_length"])
     lse = gpu[1].cpu().numpy()
@@ -144,9 +150,9 @@ def _check_full(w, what, extra_rows=()):
 
 
 @pytest.mark.parametrize("with_len", [False, True])
-def test_ramp_config_sampled(with_len):
+def test_ramp_config_all_rows(with_len):
     w = W.ramp(with_len=with_len)
-    _check_full(w, f"ramp len={with_len}")
+    _check_full(w, f"ramp len={with_len}", "ramp")
 
 
 def test_ramp_len_vs_no_len_bit_identical():
@@ -157,13 +163,16 @@ def test_ramp_len_vs_no_len_bit_identical():
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
-def test_full_config_sampled():
-    _check_full(W.full(), "full")
+def test_full_config_sampled_rows():
+    w = W.full()
+    rng = np.random.default_rng(1234)
+    rows = set(rng.choice(w["q"].shape[0], size=1024, replace=False).tolist()) | {0, 1, w["q"].shape[0] - 1}
+    _check_full(w, "full", "full", rows=np.array(sorted(rows), np.int64))
 
 
-def test_scattered_config_sampled():
+def test_scattered_config_all_rows():
     w = W.scattered()
-    _check_full(w, "scattered", extra_rows=w["empty_rows"][:4])
+    _check_full(w, "scattered", "scattered")
 
 
 @pytest.mark.parametrize("dynamic", [True, False])
