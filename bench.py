@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--skip-e2e", action="store_true", help="no host-buffer end-to-end leg")
     ap.add_argument("--skip-decode", action="store_true", help="no decode fixed-vs-dynamic leg")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--shard", choices=["replicas", "rows"], default="replicas",
+                    help="multi-GPU: every rank runs its own batch (replicas, weak scaling) or its "
+                         "contiguous rows of one batch (rows, strong scaling; flat workloads only)")
     return ap.parse_args()
 
 
@@ -354,6 +357,19 @@ def cpu_baseline(w, name, budget_s=12.0):
             "sample": f"{done} random rows of the {name} batch ({t_total:.1f} s of fp64 CPU work)"}
 
 
+def shard_rows(w, rank, world):
+    """This rank's contiguous rows of a flat workload (query rows are independent; the shared KV
+    is whole on every rank)."""
+    from sparse_mla_attention_fwd_gb300 import row_shard
+    s_q = w["q"].shape[0]
+    r0, r1 = row_shard(s_q, rank, world)
+    out = dict(w)
+    for k in ("q", "indices", "topk_length", "valid_counts"):
+        if out.get(k) is not None:
+            out[k] = np.ascontiguousarray(out[k][r0:r1])
+    return out, (r0, r1)
+
+
 def decode_fixed_vs_dynamic(smla, torch, dev, stream, flush, n=30):
     """The paged decode shape (256 requests, h_q 128, d_qk 576, 64-token pages, topk 2048) in its
     two forms, timed interleaved on the device: dynamic = the first 1024 slots valid, an INT_MAX
@@ -433,6 +449,10 @@ def main():
     w = make_workload(args.config, args.with_len)
     if args.config == "bwd":
         return main_bwd(args, w, world, rank, local, dev, barrier)
+    row_split = args.shard == "rows" and world > 1 and not w.get("paged")
+    shard = None
+    if row_split:
+        w, shard = shard_rows(w, rank, world)
     s_q, h_q, d_qk = w["q"].shape
     flops = valid_flops(w)
 
@@ -499,7 +519,7 @@ def main():
     clocks = sampler.stop(t0, t1)
     total_ms = max_over_ranks(float(np.sum(step_ms)), dev)
     ms_per_step = total_ms / args.steps
-    job_flops = sum_over_ranks(flops, dev)      # every rank runs its own batch of this shape
+    job_flops = sum_over_ranks(flops, dev)      # replicas: every rank its own batch; rows: its slice
     value = job_tflops(job_flops * args.steps, total_ms)
     launches = args.steps * launches_per_call
 
@@ -589,12 +609,15 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": (value / base) if base else None, "dtype": "bf16",
+        "scaling": "strong" if row_split else "weak", "vs_baseline": (value / base) if base else None,
+        "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": describe(w, args.config),
                    "topk_length": "passed" if (args.with_len or w["topk_length"] is not None) else "omitted",
                    "l2": "flushed (256 MB write) between timed iterations", "n_split": n_split,
                    "pct_of_bf16_peak": 100.0 * achieved / peak,
+                   "parallelism": (f"rows split over {world} GPUs (rank 0: rows {shard[0]}..{shard[1]})" if row_split
+                                   else f"{world} replica(s), one batch per GPU"),
                    "vs_baseline_ref": "FlashMLA PR #196 B200 number (other hardware, context)" if base else None},
         "roofline": roof,
         "clocks": clocks,

@@ -26,7 +26,7 @@ from ._native import EXPORTED, SmlaError, load_library, status_string
 from .native_build import LIB_PATH, build as build_library
 
 __all__ = ["sparse_mla_fwd", "sparse_mla_fwd_paged", "sparse_mla_fwd_paged_splitkv_static", "sparse_mla_fwd_host",
-           "auto_splits",
+           "row_shard", "sparse_mla_fwd_sharded", "auto_splits",
            "sparse_mla_bwd", "sparse_mla_device_status",
            "sparse_mla_status_string", "SmlaError", "load_library", "build_library", "LIB_PATH"]
 
@@ -133,6 +133,30 @@ def sparse_mla_fwd_host(q, kv, indices, topk_length=None, attn_sink=None, sm_sca
     if rc != 0:
         raise SmlaError(rc, "sparse_mla_fwd_host")
     return out, lse, max_logits
+
+
+def row_shard(s_q, rank, world):
+    """The contiguous query rows [r0, r1) that rank `rank` of `world` owns in a batch of s_q rows.
+    Rows are independent, so a batch splits across GPUs with no exchange; the first s_q % world
+    ranks take one row more."""
+    if world < 1 or not 0 <= rank < world or s_q < 0:
+        raise ValueError("need 0 <= rank < world and s_q >= 0")
+    base, extra = divmod(int(s_q), int(world))
+    r0 = rank * base + min(rank, extra)
+    return r0, r0 + base + (1 if rank < extra else 0)
+
+
+def sparse_mla_fwd_sharded(q, kv, indices, rank, world, topk_length=None, attn_sink=None, sm_scale=None,
+                           d_v=512, stream=None, n_split=1):
+    """The forward on this rank's rows of the batch (see row_shard): every GPU holds the whole
+    shared KV and the batch's tensors, computes its own contiguous rows, and keeps its outputs
+    (an all-gather is needed only if a caller wants them replicated).  Returns (r0, r1) and the
+    outputs of those rows."""
+    r0, r1 = row_shard(q.shape[0], rank, world)
+    tl = None if topk_length is None else topk_length[r0:r1]
+    out = sparse_mla_fwd(q[r0:r1], kv, indices[r0:r1], tl, attn_sink, sm_scale=sm_scale, d_v=d_v,
+                         stream=stream, n_split=n_split)
+    return (r0, r1), out
 
 
 def auto_splits(s_q, h_q, topk, device=None):

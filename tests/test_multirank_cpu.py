@@ -2,7 +2,9 @@
 
 Every rank runs its own batch (weak scaling, no collective on the data path); the only
 exchanges are the max of the ranks' times and the sum of their work, taken after the timed
-region.  The reference arm runs on rank 0 alone.
+region.  The reference arm runs on rank 0 alone.  A batch can also be split by rows across the
+ranks (row_shard): the shards partition the rows, and the per-shard results are exactly the
+rows of the whole batch's result.
 """
 import os
 import socket
@@ -73,3 +75,61 @@ def test_single_process_needs_no_group():
     assert not dist.is_initialized()
     assert bench.max_over_ranks(3.5) == 3.5 and bench.sum_over_ranks(2.0) == 2.0
     assert bench.job_tflops(1.0337e12, 1.078) == pytest.approx(958.9, rel=1e-3)
+
+
+def _shard_main(rank, world, port, result_q):
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import numpy as np
+    import oracle
+    import workloads as W
+    from sparse_mla_attention_fwd_gb300 import row_shard
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = W.random_case(61, 23, 300, 64, 512, 90, with_len=True, with_sink=True)
+        r0, r1 = row_shard(23, rank, world)
+        # each rank computes its own rows only (the oracle stands in for the GPU here)
+        out, lse, mx = oracle.sparse_mla_fwd(w["q"], w["kv"], w["indices"], w["topk_length"], w["attn_sink"],
+                                             w["sm_scale"], rows=np.arange(r0, r1), threads=1)
+        gathered = [None] * world
+        dist.all_gather_object(gathered, (rank, r0, r1, lse.tolist()))
+        result_q.put((rank, r0, r1, gathered))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_row_shards_partition_the_batch_and_reproduce_it(world):
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import oracle
+    import workloads as W
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    gathered = sorted(results[0][3])
+    edges = [(r0, r1) for _, r0, r1, _ in gathered]
+    assert edges[0][0] == 0 and edges[-1][1] == 23
+    assert all(a[1] == b[0] for a, b in zip(edges, edges[1:]))          # contiguous, disjoint
+    assert max(r1 - r0 for r0, r1 in edges) - min(r1 - r0 for r0, r1 in edges) <= 1
+    w = W.random_case(61, 23, 300, 64, 512, 90, with_len=True, with_sink=True)
+    _, lse_all, _ = oracle.sparse_mla_fwd(w["q"], w["kv"], w["indices"], w["topk_length"], w["attn_sink"],
+                                          w["sm_scale"], threads=1)
+    stitched = np.concatenate([np.array(l) for _, _, _, l in gathered])
+    assert np.array_equal(stitched, lse_all)
+
+
+def test_row_shard_edges():
+    from sparse_mla_attention_fwd_gb300 import row_shard
+    assert [row_shard(10, r, 4) for r in range(4)] == [(0, 3), (3, 6), (6, 8), (8, 10)]
+    assert row_shard(0, 0, 2) == (0, 0) and row_shard(3, 2, 5) == (2, 3) and row_shard(3, 3, 5) == (3, 3)
+    with pytest.raises(ValueError):
+        row_shard(5, 2, 2)
