@@ -58,7 +58,7 @@ def parse():
                     help="split-KV ranges per row: 'auto' (split only when items < SMs) or an integer")
     ap.add_argument("--with-len", action="store_true", help="pass topk_length in the timed steps")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--e2e-chunks", type=int, default=8, help="row chunks of the host-buffer end-to-end leg")
+    ap.add_argument("--e2e-chunks", type=int, default=16, help="row chunks of the host-buffer end-to-end leg")
     ap.add_argument("--skip-cpu", action="store_true", help="no CPU-oracle baseline leg")
     ap.add_argument("--skip-e2e", action="store_true", help="no host-buffer end-to-end leg")
     ap.add_argument("--skip-decode", action="store_true", help="no decode fixed-vs-dynamic leg")
