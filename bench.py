@@ -523,16 +523,20 @@ def main():
     value = job_tflops(job_flops * args.steps, total_ms)
     launches = args.steps * launches_per_call
 
-    # the same rows with topk_length passed (padding-overhead check), non-paged ramp only
+    # the same rows with topk_length passed (padding-overhead check), non-paged ramp only: the
+    # two forms alternate call by call, and the gap is taken between their medians
     extra = {}
     if args.config == "ramp":
         counts = torch.from_numpy(w["valid_counts"]).to(dev)
-        other = timed_steps(max(20, args.steps // 3), tl=(None if args.with_len else counts))
-        launches += len(other) * launches_per_call
-        ms_other = float(np.mean(other))
-        ms_no_len, ms_len = (ms_other, ms_per_step) if args.with_len else (ms_per_step, ms_other)
+        no_len, with_len = [], []
+        for _ in range(max(20, args.steps // 3)):
+            no_len += timed_steps(1, tl=None)
+            with_len += timed_steps(1, tl=counts)
+        launches += (len(no_len) + len(with_len)) * launches_per_call
+        ms_no_len, ms_len = float(np.median(no_len)), float(np.median(with_len))
         extra = {"ms_no_topk_length": ms_no_len, "ms_topk_length_passed": ms_len,
                  "padding_gap_pct": 100.0 * (ms_no_len - ms_len) / ms_len,
+                 "padding_gap_how": f"medians of {len(no_len)} interleaved calls of each form",
                  "valid_token_tflop": flops / 1e12}
 
     # the decode shape's fixed-width run against its dynamic-length run (default run only)

@@ -1,7 +1,8 @@
-"""The host-buffer entry point (sparse_mla_fwd_host): inputs and outputs in pinned host memory,
-copies pipelined over row chunks on their own streams.  Rows are independent, so every chunking
-must give the same bits as one device call on the whole batch; the device call itself is
-checked against the oracle."""
+"""The host-buffer entry point (sparse_mla_fwd_host: inputs and outputs in pinned host memory,
+copies pipelined over row chunks on their own streams) and the row-sharded forward
+(sparse_mla_fwd_sharded).  Rows are independent, so every chunking and every sharding must give
+the same bits as one device call on the whole batch; the device call itself is checked against
+the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -47,3 +48,24 @@ def test_host_entry_ramp_shape_in_chunks():
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref[0].cpu().view(torch.int16))
     assert torch.equal(lse, ref[1].cpu()) and torch.equal(mx, ref[2].cpu())
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_row_sharded_forward_equals_one_call(world):
+    # each rank's contiguous rows of one batch, computed alone, are exactly those rows of the
+    # whole batch's result (rows are independent)
+    w = W.random_case(78, 41, 1500, 128, 576, 260, with_len=True, with_sink=True, poison_suffix=True)
+    from gpu_helpers import dev_tensor
+    ref = run_gpu(w)
+    q, kv, idx = dev_tensor(w["q"]), dev_tensor(w["kv"]), dev_tensor(w["indices"])
+    tl, sink = dev_tensor(w["topk_length"]), dev_tensor(w["attn_sink"])
+    seen = 0
+    for rank in range(world):
+        (r0, r1), (out, lse, mx) = smla.sparse_mla_fwd_sharded(q, kv, idx, rank, world, topk_length=tl,
+                                                               attn_sink=sink, sm_scale=w["sm_scale"])
+        torch.cuda.synchronize()
+        assert r0 == seen
+        seen = r1
+        assert torch.equal(out.view(torch.int16), ref[0][r0:r1].view(torch.int16))
+        assert torch.equal(lse, ref[1][r0:r1]) and torch.equal(mx, ref[2][r0:r1])
+    assert seen == 41
