@@ -174,8 +174,9 @@ smla_status sparse_mla_fwd_paged_splitkv_static(
  *   copy_in      stream of the host -> device copies (kv and attn_sink first, then each chunk)
  *   copy_out     stream of the device -> host copies
  * The copies start after the work already queued on `stream`, so the call is ordered on
- * `stream` as a whole.  The three streams are ordered with CUDA events that the call creates
- * and releases (no memory is allocated).  The call only enqueues work; synchronise `stream` before reading
+ * `stream` as a whole.  The three streams are ordered with CUDA events from a pool that the
+ * first call on a device creates and keeps until exit (no memory is allocated); calls from
+ * several host threads take turns while they enqueue.  The call only enqueues work; synchronise `stream` before reading
  * the host outputs.  Every argument is checked before anything is enqueued; SMLA_ERR_LAUNCH
  * (a failed copy, event or launch) can come after earlier chunks were enqueued.
  */

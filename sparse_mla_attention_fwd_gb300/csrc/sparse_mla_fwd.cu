@@ -1306,15 +1306,27 @@ smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_host, const i
     return SMLA_ERR_MISALIGNED;
   const int64_t rows_per = (s_q + n_chunks - 1) / n_chunks;
   const int chunks = static_cast<int>((s_q + rows_per - 1) / rows_per);
-  // events order the three streams: inputs of chunk i -> its kernel -> its outputs
-  cudaEvent_t ev[2 * kMaxHostChunks + 3];
-  const int n_ev = 2 * chunks + 3;
-  for (int e = 0; e < n_ev; ++e) {
-    if (cudaEventCreateWithFlags(&ev[e], cudaEventDisableTiming) != cudaSuccess) {
-      for (int k = 0; k < e; ++k) cudaEventDestroy(ev[k]);
-      return SMLA_ERR_LAUNCH;
+  // Events order the three streams: inputs of chunk i -> its kernel -> its outputs.  They come
+  // from a pool per device, created on the first call there; re-recording an event is safe for
+  // the waits enqueued earlier, and the lock keeps two host threads from recording the same
+  // events at once while they enqueue.
+  constexpr int kEvents = 2 * kMaxHostChunks + 3;
+  static std::mutex pool_mu;
+  static cudaEvent_t pool[64][kEvents];
+  static bool pool_ready[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SMLA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(pool_mu);
+  if (!pool_ready[dev]) {
+    for (int e = 0; e < kEvents; ++e) {
+      if (cudaEventCreateWithFlags(&pool[dev][e], cudaEventDisableTiming) != cudaSuccess) {
+        for (int k = 0; k < e; ++k) cudaEventDestroy(pool[dev][k]);
+        return SMLA_ERR_LAUNCH;
+      }
     }
+    pool_ready[dev] = true;
   }
+  cudaEvent_t* ev = pool[dev];
   cudaEvent_t ev_kv = ev[0], ev_done = ev[1], ev_start = ev[2];
   auto ev_in = [&](int i) { return ev[3 + 2 * i]; };
   auto ev_k = [&](int i) { return ev[4 + 2 * i]; };
@@ -1360,7 +1372,6 @@ smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_host, const i
   // the caller's stream completes only after the last copy out
   ok = ok && cudaEventRecord(ev_done, copy_out) == cudaSuccess;
   ok = ok && cudaStreamWaitEvent(stream, ev_done, 0) == cudaSuccess;
-  for (int e = 0; e < n_ev; ++e) cudaEventDestroy(ev[e]);   // released once they complete
   if (st != SMLA_OK) return st;
   return ok ? SMLA_OK : SMLA_ERR_LAUNCH;
 }
