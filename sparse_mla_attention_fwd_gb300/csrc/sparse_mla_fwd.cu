@@ -804,10 +804,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S buffer s was last read by the softmax of block b-2
             if (b >= 2) wait_or_flag(smem_u32(&bar_p_full[s]), ((b - 2) >> 1) & 1, abort, lim);
             const uint64_t kd0 = make_sdesc_sw128(kv_base + s * kTileBytes, 16, 1024);
-            // S = QK^T group by group, as the column groups of the stage land
+            // S = QK^T group by group, as the column groups of the stage land.  Groups 0 and 1
+            // are waited for together: starting on group 0 while group 1 is still landing measured
+            // ~1 % slower (more of the operand reads then overlap the fill of the same stage).
 #pragma unroll
             for (int g = 0; g < kGroups; ++g) {
-              wait_or_flag(smem_u32(&bar_kv_full[s][g]), (b >> 1) & 1, abort, lim);
+              if (g == 0) {
+                wait_or_flag(smem_u32(&bar_kv_full[s][0]), (b >> 1) & 1, abort, lim);
+                wait_or_flag(smem_u32(&bar_kv_full[s][1]), (b >> 1) & 1, abort, lim);
+              } else if (g > 1) {
+                wait_or_flag(smem_u32(&bar_kv_full[s][g]), (b >> 1) & 1, abort, lim);
+              }
               tc_fence_after();
               if (g == 0) SMLA_TRACE_EVENT(b, kTrQkIssue);
               const int ks_end = (g == kGroups - 1) ? kQkSteps : 8 * (g + 1);
