@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import subprocess
 import sys
 import time
@@ -338,7 +339,8 @@ def run_reference(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": describe(w, args.config), "topk_length": "passed" if w["topk_length"] is not None else "omitted"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -354,6 +356,18 @@ def _oracle_call(oracle, w, rows):
                                            w["topk_length"], w["attn_sink"], w["sm_scale"], w["d_v"], rows=rows)
     return oracle.sparse_mla_fwd(w["q"], w["kv"], w["indices"], w["topk_length"], w["attn_sink"],
                                  w["sm_scale"], w["d_v"], rows=rows)
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu's "Model name", else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
 
 
 def cpu_baseline(w, name, budget_s=12.0):
@@ -374,7 +388,7 @@ def cpu_baseline(w, name, budget_s=12.0):
         t_total += time.perf_counter() - t0
         flops += valid_flops(w, rows, backward=bool(w.get("backward")))
         done += len(rows)
-    return {"value": flops / t_total / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": flops / t_total / 1e12, "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
             "sample": f"{done} random rows of the {name} batch ({t_total:.1f} s of fp64 CPU work)"}
 
 
