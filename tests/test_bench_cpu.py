@@ -76,3 +76,21 @@ def test_paged_bytes_read_every_gathered_row():
               + gather + s_q * h_q * w["d_v"] * 2 + 2 * s_q * h_q * 4)
     assert gather == _counted(w) * d_qk * 2
     assert hbm == expect
+
+
+def test_counters_are_used_only_for_the_kernel_source_they_were_taken_on(monkeypatch):
+    entry = bench.profiled_counters("ramp")
+    if entry:
+        assert entry["kernel_source_hash"] == bench.kernel_source_hash("fwd")
+        assert entry["dram_bytes_per_launch"] > 0
+    # any other source: no counters, so the bench line reports traffic as unknown
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel="fwd": "0" * 16)
+    for name in ("ramp", "decode", "full", "scattered", "bwd"):
+        assert bench.profiled_counters(name) == {}
+    assert bench.profiled_counters("no_such_workload") == {}
+
+
+def test_kernel_source_hash_covers_the_backward_file_only_for_the_backward():
+    fwd, bwd = bench.kernel_source_hash("fwd"), bench.kernel_source_hash("bwd")
+    assert len(fwd) == 16 and len(bwd) == 16 and fwd != bwd
+    int(fwd, 16), int(bwd, 16)
