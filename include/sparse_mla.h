@@ -176,9 +176,10 @@ smla_status sparse_mla_fwd_paged_splitkv_static(
  * The copies start after the work already queued on `stream`, so the call is ordered on
  * `stream` as a whole.  The three streams are ordered with CUDA events from a pool that the
  * first call on a device creates and keeps until exit (no memory is allocated); calls from
- * several host threads take turns while they enqueue.  The call only enqueues work; synchronise `stream` before reading
- * the host outputs.  Every argument is checked before anything is enqueued; SMLA_ERR_LAUNCH
- * (a failed copy, event or launch) can come after earlier chunks were enqueued.
+ * several host threads take turns while they enqueue.  The call only enqueues work:
+ * synchronise `stream` before reading the host outputs.  Every argument is checked before
+ * anything is enqueued; SMLA_ERR_LAUNCH (a failed copy, event or launch) can come after
+ * earlier chunks were enqueued.
  */
 smla_status sparse_mla_fwd_host(const void* q_host, const void* kv_host, const int32_t* indices_host,
                                 const int32_t* topk_length_host, const float* attn_sink_host, float sm_scale,
