@@ -289,6 +289,14 @@ def test_paged_per_request_lengths(with_len):
     assert_parity(to_np(run_gpu(w)), run_oracle(w), f"paged seqlens len={with_len}")
 
 
+@pytest.mark.parametrize("page, max_blocks, h_q, d_qk", [(1, 400, 64, 512), (48, 9, 128, 576), (100, 5, 192, 512)])
+def test_paged_page_sizes(page, max_blocks, h_q, d_qk):
+    # one-token pages, and page sizes that are not powers of two: the position -> (page, row)
+    # split is plain integer division on both sides
+    w = _paged_case(50 + page, page=page, max_blocks=max_blocks, h_q=h_q, d_qk=d_qk)
+    assert_parity(to_np(run_gpu(w)), run_oracle(w), f"paged page={page} h_q={h_q} d_qk={d_qk}")
+
+
 def _paged_edge_case(seed, n_req=5, s_q_per_req=2, page=64, max_blocks=6, h_q=64, d_qk=576, topk=520):
     """Paged cache whose requests are longer than their block-table rows (positions past the
     table), with unmapped (negative) table entries and pages that run off the end of the pool."""
