@@ -289,6 +289,26 @@ def test_paged_per_request_lengths(with_len):
     assert_parity(to_np(run_gpu(w)), run_oracle(w), f"paged seqlens len={with_len}")
 
 
+def test_kv_rows_past_2_gib():
+    # a 2.5 M-row KV (2.9 GB): half of every row's slots point past byte offset 2^31 of the KV,
+    # one of them at its very last row; only the referenced rows carry data
+    rng = np.random.default_rng(77)
+    s_kv, s_q, h_q, d_qk, topk = 2_500_000, 6, 64, 576, 256
+    high = np.arange(s_kv - 2000, s_kv)
+    assert int(high[0]) * d_qk * 2 > 2 ** 31
+    idx = np.empty((s_q, 1, topk), np.int32)
+    for i in range(s_q):
+        row = np.concatenate([rng.choice(high, size=topk // 2, replace=False),
+                              rng.choice(s_kv - 2000, size=topk // 2, replace=False)])
+        idx[i, 0] = rng.permutation(row)
+    idx[0, 0, 0] = s_kv - 1
+    kv = np.zeros((s_kv, 1, d_qk), np.uint16)
+    used = np.unique(idx)
+    kv[used] = W.normal_bf16(rng, (len(used), 1, d_qk))
+    w = W._base("kv_past_2gib", W.normal_bf16(rng, (s_q, h_q, d_qk)), kv, idx, s_kv=s_kv)
+    assert_parity(to_np(run_gpu(w)), run_oracle(w), "kv rows past 2 GiB")
+
+
 @pytest.mark.parametrize("page, max_blocks, h_q, d_qk", [(1, 400, 64, 512), (48, 9, 128, 576), (100, 5, 192, 512)])
 def test_paged_page_sizes(page, max_blocks, h_q, d_qk):
     # one-token pages, and page sizes that are not powers of two: the position -> (page, row)
