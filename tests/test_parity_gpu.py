@@ -289,6 +289,13 @@ def test_paged_per_request_lengths(with_len):
     assert_parity(to_np(run_gpu(w)), run_oracle(w), f"paged seqlens len={with_len}")
 
 
+@pytest.mark.parametrize("with_len", [False, True])
+def test_very_long_lists(with_len):
+    # 40000-slot lists (up to 625 blocks in one row, slot numbers past 2^15), mixed row kinds
+    w = W.random_case(91, 4, 70000, 64, 512, 40000, with_len=with_len, poison_suffix=with_len)
+    assert_parity(to_np(run_gpu(w)), run_oracle(w), f"very long lists len={with_len}")
+
+
 def test_kv_rows_past_2_gib():
     # a 2.5 M-row KV (2.9 GB): half of every row's slots point past byte offset 2^31 of the KV,
     # one of them at its very last row; only the referenced rows carry data
