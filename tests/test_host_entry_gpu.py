@@ -39,6 +39,17 @@ def test_host_entry_equals_device_call(n_chunks, with_len):
         assert_parity(to_np(ref), run_oracle(w), f"device call len={with_len}")
 
 
+def test_host_entry_with_an_empty_kv():
+    # s_kv == 0: nothing to copy for kv, and every row is empty (O = 0, lse = +inf, max = -inf)
+    w = W.random_case(80, 11, 40, 128, 576, 24, with_sink=True)
+    w = dict(w, kv=w["kv"][:0])
+    out, lse, mx = smla.sparse_mla_fwd_host(_host(w["q"]), _host(w["kv"]), _host(w["indices"]),
+                                            attn_sink=_host(w["attn_sink"]), sm_scale=w["sm_scale"],
+                                            n_chunks=4)
+    torch.cuda.synchronize()
+    assert torch.all(out.float() == 0) and torch.all(lse == float("inf")) and torch.all(mx == float("-inf"))
+
+
 def test_host_entry_ramp_shape_in_chunks():
     # the benchmark's batch through the host entry, as bench.py's end-to-end leg runs it
     w = W.ramp()
