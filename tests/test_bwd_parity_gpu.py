@@ -59,6 +59,8 @@ CASES = [
     (3, 24, 5000, 64, 576, 1024, False, True, False),
     (4, 32, 333, 64, 512, 64, True, True, True),
     (5, 16, 2000, 128, 576, 96, True, False, False),
+    (6, 10, 50, 192, 576, 1, True, True, False),        # one slot per row, three head groups
+    (7, 12, 3000, 256, 512, 2500, False, True, True),   # 40 blocks per row, four head groups
 ]
 
 
